@@ -1,0 +1,199 @@
+"""CPU oracle for the quantized paged KV store -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package.  The product (``quantized_paged_kv_store_gb300``)
+never imports it, and this package never imports the product.  The arithmetic
+lives in ``kvq_oracle.c`` (plain C, fp64 attention, nearest-code encoding);
+this module compiles it with gcc and marshals numpy arrays into it.
+
+Cited sources and the readings taken where the pages are silent are listed at
+the top of ``kvq_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvq_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+FORMATS = {"bf16": 0, "fp8_e4m3": 1, "fp8_e5m2": 2, "fp4_mx_block16": 3, "nvfp4": 4}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile kvq_oracle.c into a shared library (gcc, OpenMP, no FP contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-Wextra", "-Wno-unused-parameter", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            u32, i32, i64, f64, vp = (ctypes.c_uint32, ctypes.c_int, ctypes.c_int64,
+                                      ctypes.c_double, ctypes.c_void_p)
+            for name in ("orc_dec_e4m3", "orc_dec_e5m2", "orc_dec_e2m1", "orc_dec_e8m0",
+                         "orc_dec_bf16"):
+                getattr(lib, name).argtypes = [u32]
+                getattr(lib, name).restype = f64
+            for name in ("orc_enc_e4m3", "orc_enc_e5m2", "orc_enc_e2m1"):
+                getattr(lib, name).argtypes = [f64]
+                getattr(lib, name).restype = u32
+            lib.orc_enc_bf16.argtypes = [ctypes.c_float]
+            lib.orc_enc_bf16.restype = u32
+            lib.orc_bytes_per_token.argtypes = [i32, i32, i32, i32]
+            lib.orc_bytes_per_token.restype = i64
+            lib.orc_quantize_store.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, i32, vp,
+                                               vp, vp, vp, vp]
+            lib.orc_quantize_store.restype = i32
+            lib.orc_dequantize.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp, i32,
+                                           vp, vp]
+            lib.orc_dequantize.restype = i32
+            lib.orc_decode_attention.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp,
+                                                 i32, vp, i32, vp, i32, vp, i32, f64, vp]
+            lib.orc_decode_attention.restype = i32
+            lib.orc_num_threads.argtypes = []
+            lib.orc_num_threads.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _fmt(fmt) -> int:
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+# --- scalar codecs ---------------------------------------------------------
+
+def dec_e4m3(code: int) -> float:
+    return _load().orc_dec_e4m3(code)
+
+
+def dec_e5m2(code: int) -> float:
+    return _load().orc_dec_e5m2(code)
+
+
+def dec_e2m1(code: int) -> float:
+    return _load().orc_dec_e2m1(code)
+
+
+def dec_e8m0(code: int) -> float:
+    return _load().orc_dec_e8m0(code)
+
+
+def dec_bf16(bits: int) -> float:
+    return _load().orc_dec_bf16(bits)
+
+
+def enc_e4m3(v: float) -> int:
+    return _load().orc_enc_e4m3(v)
+
+
+def enc_e5m2(v: float) -> int:
+    return _load().orc_enc_e5m2(v)
+
+
+def enc_e2m1(v: float) -> int:
+    return _load().orc_enc_e2m1(v)
+
+
+def enc_bf16(v: float) -> int:
+    return _load().orc_enc_bf16(v)
+
+
+def bytes_per_token(fmt, layers: int, kv_heads: int, head_dim: int) -> int:
+    return _load().orc_bytes_per_token(_fmt(fmt), layers, kv_heads, head_dim)
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+# --- cache model ------------------------------------------------------------
+
+def data_row_bytes(fmt, head_dim: int) -> int:
+    f = _fmt(fmt)
+    return head_dim * 2 if f == 0 else (head_dim if f in (1, 2) else head_dim // 2)
+
+
+class OracleCache:
+    """Host model of one layer of the paged cache (R7 layout)."""
+
+    def __init__(self, fmt, kv_heads: int, head_dim: int, page_size: int, num_pages: int):
+        self.fmt = _fmt(fmt)
+        self.H, self.D, self.P, self.num_pages = kv_heads, head_dim, page_size, num_pages
+        rows = num_pages * kv_heads * page_size
+        rb = data_row_bytes(self.fmt, head_dim)
+        self.k_data = np.zeros((rows, rb), np.uint8)
+        self.v_data = np.zeros((rows, rb), np.uint8)
+        self.k_scales = np.zeros((rows, head_dim // 16), np.uint8)
+        self.v_scales = np.zeros((rows, head_dim // 16), np.uint8)
+        self.scales = np.ones(2, np.float32)
+
+    def quantize_store(self, k_bf16: np.ndarray, v_bf16: np.ndarray, slots: np.ndarray,
+                       scales=None) -> int:
+        """k, v: uint16 bf16 bits [n][H][D]; slots int64 [n]."""
+        k = np.ascontiguousarray(k_bf16, dtype=np.uint16)
+        v = np.ascontiguousarray(v_bf16, dtype=np.uint16)
+        s = np.ascontiguousarray(slots, dtype=np.int64)
+        if scales is not None:
+            self.scales = np.asarray(scales, np.float32).copy()
+        n = s.shape[0]
+        assert k.shape == (n, self.H, self.D) and v.shape == k.shape
+        return _load().orc_quantize_store(self.fmt, self.H, self.D, self.P, self.num_pages,
+                                          _ptr(k), _ptr(v), _ptr(s), n, _ptr(self.scales),
+                                          _ptr(self.k_data), _ptr(self.v_data),
+                                          _ptr(self.k_scales), _ptr(self.v_scales))
+
+    def dequantize(self, slots: np.ndarray):
+        s = np.ascontiguousarray(slots, dtype=np.int64)
+        n = s.shape[0]
+        ko = np.zeros((n, self.H, self.D), np.uint16)
+        vo = np.zeros((n, self.H, self.D), np.uint16)
+        rc = _load().orc_dequantize(self.fmt, self.H, self.D, self.P, self.num_pages,
+                                    _ptr(self.k_data), _ptr(self.v_data), _ptr(self.k_scales),
+                                    _ptr(self.v_scales), _ptr(self.scales), _ptr(s), n,
+                                    _ptr(ko), _ptr(vo))
+        return ko, vo, rc
+
+    def decode_attention(self, q_bf16: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
+                         sm_scale: float, b_list=None):
+        """q: uint16 [B][Hq][D]; returns (out fp64 [B][Hq][D], rc)."""
+        q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+        pt = np.ascontiguousarray(page_table, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, Hq, D = q.shape
+        out = np.zeros((B, Hq, D), np.float64)
+        bl = None if b_list is None else np.ascontiguousarray(b_list, dtype=np.int32)
+        rc = _load().orc_decode_attention(self.fmt, self.H, self.D, self.P, self.num_pages,
+                                          _ptr(self.k_data), _ptr(self.v_data),
+                                          _ptr(self.k_scales), _ptr(self.v_scales),
+                                          _ptr(self.scales), _ptr(q), Hq, _ptr(pt), pt.shape[1],
+                                          _ptr(sl), B, _ptr(bl), 0 if bl is None else bl.shape[0],
+                                          float(sm_scale), _ptr(out))
+        return out, rc
+
+    def row_index(self, slot: int, h: int) -> int:
+        return ((slot // self.P) * self.H + h) * self.P + slot % self.P
