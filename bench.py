@@ -1,0 +1,492 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the quantized paged KV store on GB300.
+
+One step = quantize-and-store of each sequence's newest token (K and V) into
+the paged cache, then fused-dequant split-K GQA decode attention of one query
+token per sequence over the whole cache (store + decode + merge kernels).
+
+Workload (default): one Llama-3-70B-shaped layer (64 q heads, 8 kv heads,
+head_dim 128), NVFP4 cache, page size 16, batch 32 with ragged context lengths
+uniform in [24K, 32K] and random page tables ("32K ctx x 32 seqs").  The
+cache (~1.06 GB) is larger than L2 (129 MB), so no L2 flush is needed between
+steps.
+
+Prints ONE JSON line on rank 0.  Under torchrun each rank runs its own batch
+(weak scaling, no collective on the data path); the timed region is bracketed
+by a barrier and the max over ranks is taken.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--format nvfp4|fp8_e4m3|...] [--sweep FILE]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV GB/s and tokens/s at 32K ctx×32 seqs (fp8/fp4) vs HBM peak"
+FALLBACK_HBM_GBS = 6800.0   # one earlier GB300 copy-bandwidth measurement
+# Bytes per (token, kv head) of K plus V at head_dim 128.
+KV_BYTES = {"bf16": 512, "fp8_e4m3": 256, "fp8_e5m2": 256, "fp4_mx_block16": 144, "nvfp4": 144}
+DTYPE = {"bf16": "bf16 cache, f32 math", "fp8_e4m3": "e4m3 cache, f32 math",
+         "fp8_e5m2": "e5m2 cache, f32 math", "fp4_mx_block16": "e2m1+e8m0 cache, f32 math",
+         "nvfp4": "e2m1+e4m3 cache, f32 math"}
+# dram read+write bytes per decode-kernel launch from an ncu capture, keyed by
+# the hash of the decode sources it was taken on (stale hash -> null)
+NCU_TRAFFIC = {}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--format", default="nvfp4")
+    p.add_argument("--seed", type=int, default=1004)
+    p.add_argument("--sweep", default=None, help="also run the format x context x batch sweep, "
+                   "one JSON line per cell appended to this file")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, init_method="env://", rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_ms: float, per_rank_bytes: float, device=None):
+    """Whole-job throughput: all ranks' bytes over the slowest rank's time."""
+    import torch.distributed as dist
+    world = dist.get_world_size() if (dist.is_available() and dist.is_initialized()) else 1
+    ms = max_over_ranks(per_rank_ms, device)
+    return ms, per_rank_bytes * world / (ms * 1e-3) / 1e9
+
+
+# --------------------------------------------------------------------- helpers
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if k in d:
+                return float(d[k]), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for n in ("kvq_decode.cu", "kvq_codecs.cuh"):
+        with open(os.path.join(ROOT, "quantized_paged_kv_store_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    mx.append(float(c[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.remove(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def algorithmic_bytes(wl, fmt):
+    """KV bytes of every cached token + Q + O of one decode call."""
+    kv = int(wl.seq_lens.astype("int64").sum()) * wl.Hkv * KV_BYTES[fmt]
+    qo = 2 * wl.B * wl.Hq * wl.D * 2
+    return kv + qo
+
+
+def store_bytes(wl, fmt):
+    """bf16 K and V read plus cache rows written for one new token per sequence."""
+    per_row = wl.D * 2 * 2 + KV_BYTES[fmt]
+    return wl.B * wl.Hkv * per_row
+
+
+def make_workload(fmt, seed, T=None, B=None):
+    import synth
+    if T is None:
+        wl = synth.cfg4_nvfp4_70b_32k(seed=seed)
+        if fmt != "nvfp4":
+            wl.fmt = fmt
+            wl.name = wl.name.replace("nvfp4", fmt)
+        return wl
+    return synth.cfg5_sweep_cell(fmt, T, B, seed=seed)
+
+
+# --------------------------------------------------------------- oracle timing
+def oracle_time(wl, seqs, ks, vs, reps=1):
+    """Seconds the CPU oracle takes to run decode attention for `seqs` (after
+    storing their tokens, untimed), and the algorithmic bytes it processed."""
+    import numpy as np
+    import oracle
+    c = oracle.OracleCache(wl.fmt, wl.Hkv, wl.D, wl.P, wl.num_pages)
+    s = wl.scales(0)
+    for b in seqs:
+        c.quantize_store(ks[b], vs[b], wl.slots(b), s)
+    q = wl.q(0)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        c.decode_attention(q, wl.page_table, wl.seq_lens, wl.sm_scale, b_list=np.array(seqs))
+    dt = (time.perf_counter() - t0) / reps
+    nbytes = sum(int(wl.seq_lens[b]) for b in seqs) * wl.Hkv * KV_BYTES[wl.fmt] + \
+        len(seqs) * wl.Hq * wl.D * 4
+    return dt, nbytes, oracle.num_threads()
+
+
+# ------------------------------------------------------------------- our arm
+def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True):
+    import numpy as np
+    import torch
+    import quantized_paged_kv_store_gb300 as kvq
+    import synth
+
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = make_workload(fmt, args.seed + 7919 * rank, T, B)
+    ks, vs = wl.kv_all(0)
+    scales = [float(x) for x in wl.scales(0)]
+    cache = kvq.KVQCache(fmt, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
+    stream = torch.cuda.current_stream()
+    # prefill: every token but the newest of each sequence (untimed)
+    for b in range(wl.B):
+        T_b = int(wl.seq_lens[b])
+        if T_b > 1:
+            cache.quantize_and_store(0, synth_to_cuda(ks[b][:T_b - 1]), synth_to_cuda(vs[b][:T_b - 1]),
+                                     torch.from_numpy(wl.slots(b, 0, T_b - 1)).to(dev), scales)
+    new_k = np.stack([ks[b][int(wl.seq_lens[b]) - 1] for b in range(wl.B)])
+    new_v = np.stack([vs[b][int(wl.seq_lens[b]) - 1] for b in range(wl.B)])
+    new_slots = np.array([wl.slots(b, int(wl.seq_lens[b]) - 1)[0] for b in range(wl.B)], np.int64)
+    q_h = wl.q(0)
+    # device-resident step inputs
+    d_k, d_v = synth_to_cuda(new_k), synth_to_cuda(new_v)
+    d_slots = torch.from_numpy(new_slots).to(dev)
+    d_q = synth_to_cuda(q_h)
+    d_pt = torch.from_numpy(wl.page_table).to(dev)
+    d_sl = torch.from_numpy(wl.seq_lens).to(dev)
+    d_out = torch.empty_like(d_q)
+    ws = torch.empty(cache.workspace_size(wl.B, wl.Hq, wl.max_pages), dtype=torch.uint8, device=dev)
+
+    def step():
+        cache.quantize_and_store(0, d_k, d_v, d_slots, scales)
+        cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale, d_out, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if cache.device_error() != 0:
+        raise RuntimeError("device error during warm-up: " + kvq.kvq_last_error_string())
+    K = args.steps
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e_start.record(stream)
+        for i in range(K):
+            cache.quantize_and_store(0, d_k, d_v, d_slots, scales)
+            d0[i].record(stream)
+            cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale, d_out, ws)
+            d1[i].record(stream)
+        e_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    local_ms = e_start.elapsed_time(e_end) / K
+    decode_ms = statistics.fmean(d0[i].elapsed_time(d1[i]) for i in range(K))
+    if cache.device_error() != 0:
+        raise RuntimeError("device error during the timed steps: " + kvq.kvq_last_error_string())
+    dbytes = algorithmic_bytes(wl, fmt)
+    sbytes = store_bytes(wl, fmt)
+    ms, gbs = aggregate(local_ms, dbytes + sbytes, dev)
+    res = {"wl": wl, "ms": ms, "gbs": gbs, "decode_ms": decode_ms, "decode_bytes": dbytes,
+           "clocks": clk.summary(), "launches": 3 * K, "world": world}
+
+    if with_e2e:
+        # same step through the public API with pinned host buffers: H2D of the
+        # step's inputs, store + decode, D2H of the output, every step
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        h_k, h_v = pin(new_k.view(np.int16)), pin(new_v.view(np.int16))
+        h_q = pin(q_h.view(np.int16))
+        h_slots, h_pt, h_sl = pin(new_slots), pin(wl.page_table), pin(wl.seq_lens)
+        h_out = torch.empty(d_out.shape, dtype=torch.int16).pin_memory()
+        dk16, dv16, dq16 = d_k.view(torch.int16), d_v.view(torch.int16), d_q.view(torch.int16)
+        h2d = sum(t.numel() * t.element_size() for t in (h_k, h_v, h_q, h_slots, h_pt, h_sl))
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            dk16.copy_(h_k, non_blocking=True)
+            dv16.copy_(h_v, non_blocking=True)
+            dq16.copy_(h_q, non_blocking=True)
+            d_slots.copy_(h_slots, non_blocking=True)
+            d_pt.copy_(h_pt, non_blocking=True)
+            d_sl.copy_(h_sl, non_blocking=True)
+            step()
+            h_out.copy_(d_out.view(torch.int16), non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(max(3, args.warmup // 4)):
+            e2e_step()
+        Ke = max(10, min(K, 1000))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(Ke):
+            e2e_step()
+        e2e_ms_local = (time.perf_counter() - t0) * 1e3 / Ke
+        barrier()
+        e2e_ms, e2e_gbs = aggregate(e2e_ms_local, dbytes + sbytes, dev)
+        res["e2e"] = {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke}
+
+    if with_cpu and rank == 0 and world == 1:
+        seqs = list(range(min(4, wl.B)))
+        dt, nb, cores = oracle_time(wl, seqs, ks, vs)
+        res["cpu_baseline"] = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+                               "kind": "oracle",
+                               "sample": f"fp64 oracle decode attention of sequences {seqs} "
+                                         f"({sum(int(wl.seq_lens[b]) for b in seqs)} tokens x "
+                                         f"{wl.Hkv} kv heads, all {wl.Hq} q heads) of the same "
+                                         f"workload; {dt:.2f} s"}
+    cache.close()
+    return res
+
+
+def synth_to_cuda(bits):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run_ours(args):
+    import torch
+    rank, world = dist_init("nccl")
+    fmt = args.format
+    r = run_cell(args, fmt, with_cpu=not args.no_cpu_baseline)
+    wl = r["wl"]
+    peak, peak_kind = peak_hbm()
+    achieved = r["decode_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
+    h = decode_source_hash()
+    traffic = NCU_TRAFFIC.get((fmt, h))
+    line = {
+        "metric": METRIC,
+        "value": round(r["gbs"], 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(r["ms"], 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": DTYPE[fmt],
+        "data": "synthetic",
+        "config": {
+            "workload": f"{wl.name}: one Llama-3-70B-shaped layer (Hq {wl.Hq}, Hkv {wl.Hkv}, "
+                        f"head_dim {wl.D}), {fmt} cache, page_size {wl.P}, batch {wl.B}, ragged "
+                        f"context U[24K, 32K] (mean {float(wl.seq_lens.mean()):.0f}), random page "
+                        f"tables; step = store newest token + decode attention",
+            "format": fmt, "batch": wl.B, "tokens_cached": int(wl.seq_lens.sum()),
+            "l2": "no flush: the cache read each step (~%.2f GB) is larger than L2 (129 MB)"
+                  % (r["decode_bytes"] / 1e9),
+            "parallelism": f"weak: {world} independent rank(s), one batch each",
+        },
+        "tokens_per_s": round(wl.B * world / (r["ms"] * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "kernel": "decode attention (split-K kernel + LSE merge), one call",
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "bytes_per_launch": r["decode_bytes"],
+                     "ms_per_launch": round(r["decode_ms"], 5)},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if "e2e" in r:
+        line["e2e"] = r["e2e"]
+    if "cpu_baseline" in r:
+        line["cpu_baseline"] = r["cpu_baseline"]
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if args.sweep:
+        run_sweep(args)
+    barrier()
+
+
+def run_sweep(args):
+    rank, world, _ = dist_env()
+    peak, _ = peak_hbm()
+    for fmt in ("bf16", "fp8_e4m3", "fp8_e5m2", "fp4_mx_block16", "nvfp4"):
+        for T in (4096, 16384, 32768):
+            for B in (1, 8, 32):
+                a = argparse.Namespace(**vars(args))
+                a.steps = max(20, min(args.steps, 300))
+                r = run_cell(a, fmt, T=T, B=B, with_e2e=False)
+                ach = r["decode_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
+                if rank == 0:
+                    with open(args.sweep, "a") as f:
+                        f.write(json.dumps({"format": fmt, "ctx": T, "batch": B,
+                                            "decode_us": round(r["decode_ms"] * 1e3, 2),
+                                            "step_us": round(r["ms"] * 1e3, 2),
+                                            "GBps": round(ach, 1), "frac": round(ach / peak, 4),
+                                            "tokens_per_s": round(B / (r["ms"] * 1e-3), 1),
+                                            "clocks": r["clocks"]}) + "\n")
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded sample of the
+    same workload (a token prefix of one sequence, all its heads), sized so the
+    whole run stays within a few minutes."""
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    import numpy as np
+    import oracle
+    wl = make_workload(args.format, args.seed)
+    seqs = [0, 1]
+    ks, vs = [], []
+    for b in seqs:
+        k, v = wl.kv(0, b)
+        ks.append(k)
+        vs.append(v)
+    c = oracle.OracleCache(wl.fmt, wl.Hkv, wl.D, wl.P, wl.num_pages)
+    s = wl.scales(0)
+    for i, b in enumerate(seqs):
+        c.quantize_store(ks[i], vs[i], wl.slots(b), s)
+    q = wl.q(0)
+
+    def one(b, T):
+        sl = np.zeros_like(wl.seq_lens)
+        sl[b] = T
+        t0 = time.perf_counter()
+        c.decode_attention(q, wl.page_table, sl, wl.sm_scale, b_list=np.array([b]))
+        return time.perf_counter() - t0, T * wl.Hkv * KV_BYTES[wl.fmt] + wl.Hq * wl.D * 4
+
+    dt, _ = one(0, 2048)
+    budget = max(0.01, min(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    T_step = int(max(64, min(int(wl.seq_lens[0]), 2048 * budget / max(dt, 1e-6))))
+    for i in range(args.warmup):
+        one(seqs[i % 2], T_step)
+    tot_t = tot_b = 0.0
+    for i in range(args.steps):
+        t, nb = one(seqs[i % 2], T_step)
+        tot_t += t
+        tot_b += nb
+    v = tot_b / tot_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_t * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "format": wl.fmt,
+                       "sample": f"each step: {T_step}-token prefix of one sequence, all "
+                                 f"{wl.Hq} q heads"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"fp64 oracle decode attention, {T_step} tokens x "
+                                       f"{wl.Hkv} kv heads per step"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -123,56 +123,62 @@ static float bf16_to_float(uint16_t bits) {
 /* Encoding: exhaustive nearest search, ties to the even code (R2)           */
 /* ------------------------------------------------------------------------ */
 
-typedef double (*dec_fn)(uint32_t);
+
+/* Decode tables of the non-negative codes, filled once from the bit-level
+ * decoders above; the encoders search them exhaustively. */
+static double tab_e4m3[0x7F], tab_e5m2[0x7C], tab_e2m1[0x8];
+
+__attribute__((constructor)) static void build_tables(void) {
+  for (uint32_t c = 0; c <= 0x7E; ++c) tab_e4m3[c] = orc_dec_e4m3(c);
+  for (uint32_t c = 0; c <= 0x7B; ++c) tab_e5m2[c] = orc_dec_e5m2(c);
+  for (uint32_t c = 0; c <= 0x7; ++c) tab_e2m1[c] = orc_dec_e2m1(c);
+}
 
 /* Nearest non-negative code to magnitude a among codes [0, max_code]
  * (all finite, increasing with the code), ties to the even code. */
-static uint32_t nearest_code(double a, dec_fn dec, uint32_t max_code) {
+static uint32_t nearest_code(double a, const double* tab, uint32_t max_code) {
   uint32_t lo = 0, hi = max_code, c;
-  double vmax = dec(max_code);
-  if (a >= vmax) return max_code;          /* saturate (satfinite) */
+  if (a >= tab[max_code]) return max_code;   /* saturate (satfinite) */
   /* lo = largest code with value <= a, hi = smallest code with value >= a */
-  for (c = 0; c <= max_code; ++c) {
-    double v = dec(c);
-    if (v <= a && v >= dec(lo)) lo = c;
-  }
-  for (c = max_code + 1; c-- > 0;) {
-    double v = dec(c);
-    if (v >= a && v <= dec(hi)) hi = c;
-  }
-  if (dec(lo) == a) return lo;
+  for (c = 0; c <= max_code; ++c)
+    if (tab[c] <= a && tab[c] >= tab[lo]) lo = c;
+  for (c = max_code + 1; c-- > 0;)
+    if (tab[c] >= a && tab[c] <= tab[hi]) hi = c;
+  if (tab[lo] == a) return lo;
   {
-    double mid = 0.5 * (dec(lo) + dec(hi));  /* exact: both have few bits */
+    double mid = 0.5 * (tab[lo] + tab[hi]);  /* exact: both have few bits */
     if (a < mid) return lo;
     if (a > mid) return hi;
     return (lo & 1u) ? hi : lo;              /* tie: even mantissa */
   }
 }
 
-static uint32_t enc_fp8(double v, dec_fn dec, uint32_t max_code) {
+static uint32_t enc_fp8(double v, const double* tab, uint32_t max_code) {
   uint32_t sign = signbit(v) ? 0x80u : 0u;
   if (isnan(v)) return 0x7Fu | sign;
-  return nearest_code(fabs(v), dec, max_code) | sign;
+  return nearest_code(fabs(v), tab, max_code) | sign;
 }
 
-uint32_t orc_enc_e4m3(double v) { return enc_fp8(v, orc_dec_e4m3, 0x7E); }
-uint32_t orc_enc_e5m2(double v) { return enc_fp8(v, orc_dec_e5m2, 0x7B); }
+uint32_t orc_enc_e4m3(double v) { return enc_fp8(v, tab_e4m3, 0x7E); }
+uint32_t orc_enc_e5m2(double v) { return enc_fp8(v, tab_e5m2, 0x7B); }
 
 /* E2M1 has no NaN; NaN inputs are outside the contract (mapped to +-6). */
 uint32_t orc_enc_e2m1(double v) {
   uint32_t sign = signbit(v) ? 0x8u : 0u;
   if (isnan(v)) return 0x7u | sign;
-  return nearest_code(fabs(v), orc_dec_e2m1, 0x7) | sign;
+  return nearest_code(fabs(v), tab_e2m1, 0x7) | sign;
 }
 
 /* bfloat16 round-to-nearest-even of a binary32 value.  The two candidates are
  * the truncation of the value and the next bfloat16 away from zero; an
- * overflow past the largest finite value rounds to infinity as in IEEE. */
+ * overflow past the largest finite value rounds to infinity as in IEEE.
+ * Any NaN gives the canonical quiet NaN 0x7FC0 (the sign of a NaN produced by
+ * arithmetic is not portable, so it is not part of the contract). */
 uint32_t orc_enc_bf16(float v) {
   uint32_t u, lo, hi;
   double a, alo, ahi, mid;
   memcpy(&u, &v, sizeof u);
-  if (isnan(v)) return ((u >> 16) & 0x8000u) | 0x7FC0u;
+  if (isnan(v)) return 0x7FC0u;
   lo = u >> 16;
   if ((u & 0xFFFFu) == 0) return lo;
   hi = lo + 1;
@@ -226,6 +232,9 @@ static int store_one(int fmt, int H, int D, int P, int64_t num_pages, const uint
                      uint8_t* scl) {
   int bad = 0;
   size_t drow = data_row_bytes(fmt, D), srow = (size_t)D / 16;
+  /* tokens are independent when their slots are distinct (duplicate slots in
+   * one call leave unspecified which token's row is stored) */
+#pragma omp parallel for schedule(static) reduction(| : bad)
   for (int i = 0; i < num_tokens; ++i) {
     int64_t slot = slots[i];
     if (slot < 0) continue;
@@ -240,8 +249,12 @@ static int store_one(int fmt, int H, int D, int P, int64_t num_pages, const uint
         memcpy(out, row, (size_t)D * 2);
       } else if (fmt == ORC_E4M3 || fmt == ORC_E5M2) {
         for (int d = 0; d < D; ++d) {
-          float q = bf16_to_float(row[d]) / s;           /* R3: fp32 division */
-          out[d] = (uint8_t)(fmt == ORC_E4M3 ? orc_enc_e4m3(q) : orc_enc_e5m2(q));
+          float xv = bf16_to_float(row[d]);
+          float q = xv / s;                              /* R3: fp32 division */
+          if (isnan(xv))                                 /* R2: sign taken from x */
+            out[d] = (uint8_t)(0x7Fu | (signbit(xv) ? 0x80u : 0u));
+          else
+            out[d] = (uint8_t)(fmt == ORC_E4M3 ? orc_enc_e4m3(q) : orc_enc_e5m2(q));
         }
       } else {
         for (int b = 0; b < D / 16; ++b) {

@@ -1,0 +1,342 @@
+// kvq_api.cu -- host side of the C ABI declared in include/kvq.h.
+//
+// The cache object follows "SGLang PR #21954 analysis: NVFP4 KV cache", Code
+// analysis 1 (create_buffers / quantize_and_store / dequantize_prev_kv): one
+// device allocation per cache holds every layer's K and V data pools and block
+// scale planes plus a device error word; per-layer scales live on the host and
+// reach the kernels as launch arguments.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "kvq_internal.h"
+
+struct kvq_cache {
+  kvq::Geometry geo;
+  int layers;
+  int device;
+  uint8_t* base;           // single device allocation
+  size_t bytes;
+  size_t layer_data_bytes; // one K (or V) data pool of one layer
+  size_t layer_scale_bytes;
+  int* err;                // device error word
+  std::vector<float> scales;    // [layers][2]
+  std::vector<char> scales_set; // [layers]
+};
+
+namespace {
+
+thread_local char g_msg[512] = "no error";
+
+kvq_status fail(kvq_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+kvq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool valid_format(int f) { return f >= KVQ_BF16 && f <= KVQ_NVFP4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvq::LayerView view(const kvq_cache* c, int layer) {
+  kvq::LayerView L;
+  const size_t per_layer = 2 * c->layer_data_bytes + 2 * c->layer_scale_bytes;
+  uint8_t* p = c->base + per_layer * (size_t)layer;
+  L.k_data = p;
+  L.v_data = p + c->layer_data_bytes;
+  if (c->layer_scale_bytes) {
+    L.k_scales = p + 2 * c->layer_data_bytes;
+    L.v_scales = L.k_scales + c->layer_scale_bytes;
+  } else {
+    L.k_scales = L.v_scales = nullptr;
+  }
+  return L;
+}
+
+kvq_status check_device(const kvq_cache* c) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != c->device)
+    return fail(KVQ_ERR_INVALID_ARG, "cache lives on device %d but device %d is current", c->device, dev);
+  return KVQ_OK;
+}
+
+kvq_status check_layer(const kvq_cache* c, int layer) {
+  if (!c) return fail(KVQ_ERR_INVALID_ARG, "cache is NULL");
+  if (layer < 0 || layer >= c->layers)
+    return fail(KVQ_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, c->layers);
+  return KVQ_OK;
+}
+
+bool uses_scales(kvq_format f) { return f == KVQ_FP8_E4M3 || f == KVQ_FP8_E5M2 || f == KVQ_NVFP4; }
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_last_error_string(void) { return g_msg; }
+
+const char* kvq_format_name(kvq_format fmt) {
+  switch (fmt) {
+    case KVQ_BF16: return "bf16";
+    case KVQ_FP8_E4M3: return "fp8_e4m3";
+    case KVQ_FP8_E5M2: return "fp8_e5m2";
+    case KVQ_FP4_BLOCK16: return "fp4_mx_block16";
+    case KVQ_NVFP4: return "nvfp4";
+  }
+  return nullptr;
+}
+
+kvq_status kvq_format_from_name(const char* name, kvq_format* out) {
+  if (!name || !out) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
+  for (int f = KVQ_BF16; f <= KVQ_NVFP4; ++f) {
+    if (std::strcmp(name, kvq_format_name((kvq_format)f)) == 0) {
+      *out = (kvq_format)f;
+      return KVQ_OK;
+    }
+  }
+  return fail(KVQ_ERR_INVALID_ARG, "unknown format name '%s'", name);
+}
+
+size_t kvq_bytes_per_token(kvq_format fmt, int layers, int kv_heads, int head_dim) {
+  if (!valid_format(fmt) || layers <= 0 || kv_heads <= 0 || head_dim <= 0 || head_dim % 16) {
+    fail(KVQ_ERR_INVALID_ARG, "invalid arguments to kvq_bytes_per_token");
+    return 0;
+  }
+  size_t row = kvq::data_row_bytes(fmt, head_dim) + (kvq::has_block_scales(fmt) ? head_dim / 16 : 0);
+  return 2 * (size_t)layers * (size_t)kv_heads * row;
+}
+
+kvq_status kvq_create_cache(kvq_format fmt, int layers, int kv_heads, int head_dim, int page_size,
+                            int num_pages, kvq_cache** out) {
+  if (!out) return fail(KVQ_ERR_INVALID_ARG, "out is NULL");
+  if (!valid_format(fmt)) return fail(KVQ_ERR_INVALID_ARG, "unknown format %d", (int)fmt);
+  if (layers <= 0 || kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || num_pages <= 0)
+    return fail(KVQ_ERR_INVALID_ARG, "all sizes must be positive");
+  if (head_dim % 16) return fail(KVQ_ERR_INVALID_ARG, "head_dim must be a multiple of 16");
+  kvq::Geometry g;
+  g.fmt = fmt;
+  g.kv_heads = kv_heads;
+  g.head_dim = head_dim;
+  g.page_size = page_size;
+  g.num_pages = num_pages;
+  g.data_row = kvq::data_row_bytes(fmt, head_dim);
+  g.scale_row = kvq::has_block_scales(fmt) ? (size_t)head_dim / 16 : 0;
+  const size_t rows = (size_t)num_pages * kv_heads * page_size;
+  const size_t ldb = (rows * g.data_row + 255) & ~(size_t)255;
+  const size_t lsb = (rows * g.scale_row + 255) & ~(size_t)255;
+  const size_t total = (2 * ldb + 2 * lsb) * (size_t)layers + 256;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const char* fault = std::getenv("KVQ_FAULT");
+  uint8_t* base = nullptr;
+  if (fault && std::strcmp(fault, "alloc") == 0) {
+    return fail(KVQ_ERR_OOM, "device allocation of %zu bytes failed (KVQ_FAULT=alloc)", total);
+  }
+  e = cudaMalloc(&base, total);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(e == cudaErrorMemoryAllocation ? KVQ_ERR_OOM : KVQ_ERR_CUDA,
+                "cudaMalloc(%zu): %s", total, cudaGetErrorString(e));
+  }
+  e = cudaMemset(base, 0, total);
+  if (e != cudaSuccess) {
+    cudaFree(base);
+    return cuda_fail(e, "cudaMemset");
+  }
+  kvq_cache* c = new (std::nothrow) kvq_cache;
+  if (!c) {
+    cudaFree(base);
+    return fail(KVQ_ERR_OOM, "host allocation failed");
+  }
+  c->geo = g;
+  c->layers = layers;
+  c->device = dev;
+  c->base = base;
+  c->bytes = total;
+  c->layer_data_bytes = ldb;
+  c->layer_scale_bytes = lsb;
+  c->err = reinterpret_cast<int*>(base + total - 256);
+  c->scales.assign((size_t)layers * 2, 1.0f);
+  c->scales_set.assign((size_t)layers, 0);
+  *out = c;
+  return KVQ_OK;
+}
+
+kvq_status kvq_destroy_cache(kvq_cache* c) {
+  if (!c) return KVQ_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(c->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaError_t e2 = cudaFree(c->base);
+  cudaSetDevice(prev);
+  delete c;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree");
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_layout(const kvq_cache* c, int layer, void** k_data, void** v_data,
+                            void** k_scales, void** v_scales, size_t strides[4]) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  kvq::LayerView L = view(c, layer);
+  if (k_data) *k_data = L.k_data;
+  if (v_data) *v_data = L.v_data;
+  if (k_scales) *k_scales = L.k_scales;
+  if (v_scales) *v_scales = L.v_scales;
+  if (strides) {
+    const kvq::Geometry& g = c->geo;
+    strides[0] = (size_t)g.kv_heads * g.page_size * g.data_row;
+    strides[1] = (size_t)g.page_size * g.data_row;
+    strides[2] = g.data_row;
+    strides[3] = g.scale_row;
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_layer_scales(const kvq_cache* c, int layer, float out[2]) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  if (!out) return fail(KVQ_ERR_INVALID_ARG, "out is NULL");
+  if (!c->scales_set[layer]) return fail(KVQ_ERR_INVALID_ARG, "layer %d has no stored data yet", layer);
+  out[0] = c->scales[2 * layer];
+  out[1] = c->scales[2 * layer + 1];
+  return KVQ_OK;
+}
+
+kvq_status kvq_quantize_and_store(kvq_cache* c, int layer, const void* k_bf16, const void* v_bf16,
+                                  const int64_t* slot_mapping, int num_tokens, const float* scales,
+                                  kvq_stream stream) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "num_tokens < 0");
+  float s[2] = {1.0f, 1.0f};
+  if (uses_scales(c->geo.fmt) && scales) {
+    for (int i = 0; i < 2; ++i) {
+      if (!std::isfinite(scales[i]) || !(scales[i] > 0.0f))
+        return fail(KVQ_ERR_INVALID_ARG, "scales must be finite and > 0 (got %g)", (double)scales[i]);
+      s[i] = scales[i];
+    }
+  }
+  if (c->scales_set[layer]) {
+    if (uses_scales(c->geo.fmt) &&
+        (c->scales[2 * layer] != s[0] || c->scales[2 * layer + 1] != s[1]))
+      return fail(KVQ_ERR_SCALE_MISMATCH,
+                  "layer %d scales are fixed at {%g, %g}; got {%g, %g}", layer,
+                  (double)c->scales[2 * layer], (double)c->scales[2 * layer + 1], (double)s[0],
+                  (double)s[1]);
+  }
+  if (num_tokens == 0) return KVQ_OK;
+  if (!k_bf16 || !v_bf16 || !slot_mapping) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+  if (!aligned16(k_bf16) || !aligned16(v_bf16))
+    return fail(KVQ_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  if ((st = check_device(c))) return st;
+  if (!c->scales_set[layer]) {
+    c->scales[2 * layer] = s[0];
+    c->scales[2 * layer + 1] = s[1];
+    c->scales_set[layer] = 1;
+  }
+  cudaError_t e = kvq::launch_store(c->geo, view(c, layer), k_bf16, v_bf16, slot_mapping,
+                                    num_tokens, s[0], s[1], c->err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize-and-store launch");
+  return KVQ_OK;
+}
+
+kvq_status kvq_dequantize(kvq_cache* c, int layer, const int64_t* slot_mapping, int num_tokens,
+                          void* k_out_bf16, void* v_out_bf16, kvq_stream stream) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "num_tokens < 0");
+  if (num_tokens == 0) return KVQ_OK;
+  if (!slot_mapping || !k_out_bf16 || !v_out_bf16) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+  if (!aligned16(k_out_bf16) || !aligned16(v_out_bf16))
+    return fail(KVQ_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+  if ((st = check_device(c))) return st;
+  cudaError_t e = kvq::launch_dequantize(c->geo, view(c, layer), slot_mapping, num_tokens,
+                                         c->scales[2 * layer], c->scales[2 * layer + 1], k_out_bf16,
+                                         v_out_bf16, c->err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+  return KVQ_OK;
+}
+
+size_t kvq_decode_workspace_size(const kvq_cache* c, int batch, int num_q_heads, int max_pages_per_seq) {
+  if (!c || batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0) {
+    fail(KVQ_ERR_INVALID_ARG, "invalid arguments to kvq_decode_workspace_size");
+    return 0;
+  }
+  kvq::DecodePlan plan;
+  const char* why = nullptr;
+  if (!kvq::plan_decode(c->geo, batch, num_q_heads, max_pages_per_seq, c->device, &plan, &why)) {
+    fail(KVQ_ERR_UNSUPPORTED, "%s", why);
+    return 0;
+  }
+  return plan.ws_bytes;
+}
+
+kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q_bf16, int num_q_heads,
+                                const int32_t* page_table, int max_pages_per_seq,
+                                const int32_t* seq_lens, int batch, float sm_scale, void* out_bf16,
+                                void* workspace, size_t workspace_bytes, kvq_stream stream) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0)
+    return fail(KVQ_ERR_INVALID_ARG, "invalid batch / num_q_heads / max_pages_per_seq");
+  if (!std::isfinite(sm_scale)) return fail(KVQ_ERR_INVALID_ARG, "sm_scale must be finite");
+  kvq::DecodePlan plan;
+  const char* why = nullptr;
+  if (!kvq::plan_decode(c->geo, batch, num_q_heads, max_pages_per_seq, c->device, &plan, &why))
+    return fail(KVQ_ERR_UNSUPPORTED, "%s", why);
+  if (batch == 0) return KVQ_OK;
+  if (!q_bf16 || !page_table || !seq_lens || !out_bf16 || !workspace)
+    return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+  if (!aligned16(q_bf16) || !aligned16(out_bf16) || !aligned16(workspace))
+    return fail(KVQ_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
+  if (workspace_bytes < plan.ws_bytes)
+    return fail(KVQ_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, plan.ws_bytes);
+  if ((st = check_device(c))) return st;
+  const kvq_format f = c->geo.fmt;
+  const float kf = uses_scales(f) ? c->scales[2 * layer] : 1.0f;
+  const float vf = uses_scales(f) ? c->scales[2 * layer + 1] : 1.0f;
+  cudaError_t e = kvq::launch_decode(c->geo, view(c, layer), plan, q_bf16, num_q_heads, page_table,
+                                     max_pages_per_seq, seq_lens, batch, sm_scale, kf, vf, out_bf16,
+                                     workspace, c->err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+  return KVQ_OK;
+}
+
+kvq_status kvq_get_device_error(kvq_cache* c, kvq_stream stream) {
+  if (!c) return fail(KVQ_ERR_INVALID_ARG, "cache is NULL");
+  kvq_status st = check_device(c);
+  if (st) return st;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, c->err, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (word) {
+    const int zero = 0;
+    e = cudaMemcpy(c->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  }
+  if (word & kvq::kErrTimeout) return fail(KVQ_ERR_TIMEOUT, "a kernel's bounded wait ran out");
+  if (word & kvq::kErrRange)
+    return fail(KVQ_ERR_DEVICE_RANGE, "a kernel saw an out-of-range slot, page id or sequence length");
+  return KVQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// kvq_internal.h -- definitions shared by the host C-ABI and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// Bits of the device error word.
+constexpr int kErrRange = 1;    // out-of-range slot, page id or sequence length
+constexpr int kErrTimeout = 2;  // a bounded wait ran out
+
+// Rows of one layer's pool: [num_pages][kv_heads][page_size][row bytes].
+struct LayerView {
+  uint8_t* k_data;
+  uint8_t* v_data;
+  uint8_t* k_scales;  // nullptr unless the format has block scales
+  uint8_t* v_scales;
+};
+
+struct Geometry {
+  kvq_format fmt;
+  int kv_heads;
+  int head_dim;
+  int page_size;
+  int64_t num_pages;
+  size_t data_row;   // bytes per token row of a data pool
+  size_t scale_row;  // bytes per token row of a scale plane (0: none)
+};
+
+inline size_t data_row_bytes(kvq_format f, int head_dim) {
+  switch (f) {
+    case KVQ_BF16: return (size_t)head_dim * 2;
+    case KVQ_FP8_E4M3:
+    case KVQ_FP8_E5M2: return (size_t)head_dim;
+    default: return (size_t)head_dim / 2;
+  }
+}
+inline bool has_block_scales(kvq_format f) { return f == KVQ_FP4_BLOCK16 || f == KVQ_NVFP4; }
+
+// ---- launchers (defined in the .cu files; return a CUDA error code) -------
+
+cudaError_t launch_store(const Geometry& g, const LayerView& L, const void* k, const void* v,
+                         const int64_t* slots, int num_tokens, float s_k, float s_v, int* err,
+                         cudaStream_t stream);
+
+cudaError_t launch_dequantize(const Geometry& g, const LayerView& L, const int64_t* slots,
+                              int num_tokens, float s_k, float s_v, void* k_out, void* v_out,
+                              int* err, cudaStream_t stream);
+
+// Decode attention plan: how many warp workers and how much workspace.
+struct DecodePlan {
+  int group;          // q heads per kv head (G)
+  int head_groups;    // ceil(G / 8): units per (sequence, kv head)
+  int num_workers;    // warps that share the page-tile range
+  int ctas;           // thread blocks launched
+  int64_t num_units;  // batch * kv_heads * head_groups
+  int64_t num_slots;  // num_units + num_workers partial slots
+  size_t ws_bytes;    // total workspace bytes
+};
+
+// Fills `plan` for a call; returns false (with a message) if unsupported.
+bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_per_seq,
+                 int device, DecodePlan* plan, const char** why);
+
+cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePlan& plan,
+                          const void* q, int num_q_heads, const int32_t* page_table,
+                          int max_pages_per_seq, const int32_t* seq_lens, int batch,
+                          float sm_scale, float k_factor, float v_factor, void* out,
+                          void* workspace, int* err, cudaStream_t stream);
+
+}  // namespace kvq

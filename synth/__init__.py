@@ -135,25 +135,33 @@ class Workload:
         return self.page_table[b, t // self.P].astype(np.int64) * self.P + t % self.P
 
     # ---- calibration recipe (an input to both sides) -----------------------
-    def scales(self, layer: int = 0) -> np.ndarray:
-        """float32 [2]: FP8 {k_scale, v_scale} or NVFP4 {g_k, g_v} = amax / format max,
-        amax taken over every generated K (resp. V) value of the layer; 1.0 otherwise."""
-        if layer in self._scales:
-            return self._scales[layer]
+    def kv_all(self, layer: int = 0):
+        """bf16 bits K, V of every sequence (two lists), drawn once; also fixes
+        the layer's scale inputs from them."""
+        ks, vs = [], []
+        for b in range(self.B):
+            k, v = self.kv(layer, b)
+            ks.append(k)
+            vs.append(v)
+        if layer not in self._scales:
+            self._scales[layer] = self._scales_from(ks, vs)
+        return ks, vs
+
+    def _scales_from(self, ks, vs) -> np.ndarray:
         div = _CAL_DIVISOR.get(self.fmt)
         if div is None or self.scale_mode == "one":
-            s = np.ones(2, np.float32)
-        else:
-            ka = va = 0.0
-            for b in range(self.B):
-                if int(self.seq_lens[b]) == 0:
-                    continue
-                k, v = self.kv(layer, b)
-                ka = max(ka, float(np.abs(bf16_bits_to_float(k)).max()))
-                va = max(va, float(np.abs(bf16_bits_to_float(v)).max()))
-            s = np.array([ka / div if ka > 0 else 1.0, va / div if va > 0 else 1.0], np.float32)
-        self._scales[layer] = s
-        return s
+            return np.ones(2, np.float32)
+        ka = max((float(np.abs(bf16_bits_to_float(k)).max()) for k in ks if k.size), default=0.0)
+        va = max((float(np.abs(bf16_bits_to_float(v)).max()) for v in vs if v.size), default=0.0)
+        return np.array([ka / div if ka > 0 else 1.0, va / div if va > 0 else 1.0], np.float32)
+
+    def scales(self, layer: int = 0) -> np.ndarray:
+        """float32 [2]: FP8 {k_scale, v_scale} or NVFP4 {g_k, g_v} = amax / format max,
+        amax taken over every generated K (resp. V) value of the layer; 1.0 otherwise
+        (and in the default-scale mode)."""
+        if layer not in self._scales:
+            self.kv_all(layer)
+        return self._scales[layer]
 
 
 def make_page_table(seq_lens, P: int, seed: int, slack_pages: int = 0, max_pages: int | None = None):

@@ -30,3 +30,24 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def kvq():
+    """The product binding (builds libkvq.so first if it is missing)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_kvq_build", os.path.join(ROOT, "quantized_paged_kv_store_gb300", "build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    b.build()
+    import quantized_paged_kv_store_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="session")
+def cuda(kvq):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")

@@ -1,0 +1,122 @@
+"""GPU parity of decode attention against the oracle's fp64 attention on the
+same dequantized K/V: per (sequence, q head) relative L2 error <= 2e-3 and
+elementwise abs error <= 1e-2 on the bf16 output (elements with |ref| >= 4,
+where no bf16 value is within 1e-2, compare against bf16(ref))."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import (assert_attention_close, bits_to_cuda, gpu_cache_for, gpu_decode,
+                      oracle_cache_for, store_layer)
+
+pytestmark = pytest.mark.gpu
+FORMATS = ["bf16", "fp8_e4m3", "fp8_e5m2", "fp4_mx_block16", "nvfp4"]
+
+
+def _run(kvq, orc, wl, layer=0, seqs=None, **kw):
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl, layer)
+    got = gpu_decode(c, wl, layer, **kw)
+    assert c.device_error() == 0
+    oc = oracle_cache_for(orc, wl, layer, seqs=seqs)
+    ref, rc = oc.decode_attention(wl.q(layer), wl.page_table, wl.seq_lens, wl.sm_scale, b_list=seqs)
+    assert rc == 0
+    if seqs is not None:
+        got, ref = got[seqs], ref[seqs]
+    return got, ref
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (32, 8), (8, 8), (32, 2), (12, 3)])
+def test_decode_small(kvq, orc, cuda, fmt, Hq, Hkv):
+    wl = synth.make_workload(f"dec_{fmt}", fmt, Hq=Hq, Hkv=Hkv, seq_lens=[37, 1, 16, 0, 130, 17],
+                             seed=40 + Hq)
+    got, ref = _run(kvq, orc, wl)
+    assert_attention_close(got, ref, f"{fmt} Hq={Hq} Hkv={Hkv}")
+    assert (got[3] == 0).all()                            # empty sequence
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("P", [32, 64])
+def test_decode_page_sizes(kvq, orc, cuda, fmt, P):
+    wl = synth.make_workload(f"p_{fmt}", fmt, Hq=16, Hkv=4, P=P, seq_lens=[300, 65, 15], seed=7 + P)
+    got, ref = _run(kvq, orc, wl)
+    assert_attention_close(got, ref, f"{fmt} P={P}")
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "nvfp4"])
+def test_decode_many_short_sequences(kvq, orc, cuda, fmt):
+    lens = list(np.random.default_rng(1).integers(0, 40, 300))
+    wl = synth.make_workload(f"m_{fmt}", fmt, Hq=8, Hkv=2, seq_lens=lens, seed=77)
+    got, ref = _run(kvq, orc, wl)
+    assert_attention_close(got, ref, f"{fmt} 300 short sequences")
+
+
+def test_cfg1_e4m3_small(kvq, orc, cuda):
+    wl = synth.cfg1_e4m3_small()
+    got, ref = _run(kvq, orc, wl)
+    assert_attention_close(got, ref, "cfg1")
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e5m2", "fp8_e4m3"])
+@pytest.mark.parametrize("scale_mode", ["amax", "one"])
+def test_cfg2_llama8b_stack_sampled_layers(kvq, orc, cuda, fmt, scale_mode):
+    wl = synth.cfg2_llama8b_stack(fmt, scale_mode=scale_mode)
+    c = gpu_cache_for(kvq, wl)
+    for layer in range(wl.layers):
+        store_layer(c, wl, layer)
+    torch.cuda.synchronize()
+    assert c.device_error() == 0
+    for layer in (0, 31):
+        got = gpu_decode(c, wl, layer)
+        oc = oracle_cache_for(orc, wl, layer)
+        ref, rc = oc.decode_attention(wl.q(layer), wl.page_table, wl.seq_lens, wl.sm_scale)
+        assert rc == 0
+        assert_attention_close(got, ref, f"cfg2 {fmt} {scale_mode} layer {layer}")
+
+
+def test_cfg4_nvfp4_32k_full_size_sampled(kvq, orc, cuda):
+    """The benchmark's workload (70B layer, batch 32, ragged 24K-32K) in the
+    benchmark's launch configuration; two sequences checked against the oracle."""
+    wl = synth.cfg4_nvfp4_70b_32k()
+    seqs = [int(np.argmax(wl.seq_lens)), 3]
+    got, ref = _run(kvq, orc, wl, seqs=seqs)
+    assert_attention_close(got, ref, "cfg4 sampled")
+
+
+def test_decode_bad_page_and_length(kvq, cuda):
+    wl = synth.make_workload("bad", "fp8_e4m3", Hq=8, Hkv=2, seq_lens=[40, 40, 40], seed=2)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    pt = wl.page_table.copy()
+    pt[1, 1] = wl.num_pages + 3
+    got = gpu_decode(c, wl, page_table=pt)
+    assert c.device_error() == kvq._binding._STATUS_CODES["KVQ_ERR_DEVICE_RANGE"]
+    assert (got[1] == 0).all() and (got[0] != 0).any() and (got[2] != 0).any()
+    got = gpu_decode(c, wl, seq_lens=[40, wl.max_pages * wl.P + 1, -1])
+    assert c.device_error() == kvq._binding._STATUS_CODES["KVQ_ERR_DEVICE_RANGE"]
+    assert (got[1] == 0).all() and (got[2] == 0).all() and (got[0] != 0).any()
+
+
+def test_decode_deterministic_and_workspace_checks(kvq, cuda):
+    wl = synth.make_workload("det", "nvfp4", Hq=16, Hkv=2, seq_lens=[500, 77], seed=12)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    a = gpu_decode(c, wl)
+    b = gpu_decode(c, wl)
+    assert np.array_equal(a, b)
+    q = bits_to_cuda(wl.q())
+    pt = torch.from_numpy(wl.page_table).cuda()
+    sl = torch.from_numpy(wl.seq_lens).cuda()
+    n = c.workspace_size(wl.B, wl.Hq, wl.max_pages)
+    small = torch.empty(n - 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KVQError) as e:
+        c.decode_attention(0, q, pt, sl, wl.sm_scale, workspace=small)
+    assert e.value.code == "KVQ_ERR_INVALID_ARG"
+    with pytest.raises(kvq.KVQError) as e:
+        c.workspace_size(1, 17 * 2, 4)                    # group 17 > 16
+    cbad = kvq.KVQCache("fp8_e4m3", 1, 2, 64, 16, 4)     # head_dim 64: store only
+    with pytest.raises(kvq.KVQError) as e:
+        cbad.workspace_size(1, 4, 4)
+    assert e.value.code == "KVQ_ERR_UNSUPPORTED"
