@@ -74,15 +74,22 @@ def gpu_decode(cache, wl, layer=0, q_bits=None, seq_lens=None, page_table=None):
 
 
 def attention_errors(got: np.ndarray, ref: np.ndarray):
-    """Per (b, head) relative L2 error and elementwise abs error with the
-    bf16-representability rule: where |ref| >= 4 no bf16 value can be within
-    1e-2, so those elements compare against bf16(ref) instead."""
-    ref_bf16 = synth.bf16_bits_to_float(synth.to_bf16_bits(torch.from_numpy(ref.astype(np.float32))))
+    """Errors of a bf16 attention output against the fp64 reference, in excess
+    of the reference's own bf16 rounding (no bf16 output can do better than
+    bf16(ref); its rounding alone reaches ~2.3e-3 relative L2 on some vectors):
+      rel[b, j] = (||got - ref|| - ||bf16(ref) - ref||) / ||ref||
+      absd[...] = |got - ref| - |bf16(ref) - ref|
+    Also returns the raw relative L2 error (got vs ref) for reporting."""
+    ref_bf16 = synth.bf16_bits_to_float(
+        synth.to_bf16_bits(torch.from_numpy(ref.astype(np.float32)))).astype(np.float64)
+    floor = np.linalg.norm(ref_bf16 - ref, axis=-1)
     num = np.linalg.norm(got - ref, axis=-1)
     den = np.linalg.norm(ref, axis=-1)
-    rel = np.where(den > 0, num / np.where(den > 0, den, 1), num)
-    absd = np.where(np.abs(ref) >= 4, np.abs(got - ref_bf16), np.abs(got - ref))
-    return rel, absd
+    safe = np.where(den > 0, den, 1)
+    rel = np.where(den > 0, (num - floor) / safe, num)
+    raw = np.where(den > 0, num / safe, num)
+    absd = np.abs(got - ref) - np.abs(ref_bf16 - ref)
+    return rel, absd, raw
 
 
 REL_TOL = 2e-3
@@ -90,8 +97,8 @@ ABS_TOL = 1e-2
 
 
 def assert_attention_close(got, ref, where=""):
-    rel, absd = attention_errors(got, ref)
+    rel, absd, raw = attention_errors(got, ref)
     assert np.isfinite(got).all(), where
     assert rel.max() <= REL_TOL, f"{where}: max rel L2 {rel.max():.3e} at {np.unravel_index(rel.argmax(), rel.shape)}"
     assert absd.max() <= ABS_TOL, f"{where}: max abs {absd.max():.3e}"
-    return float(rel.max()), float(absd.max())
+    return float(rel.max()), float(absd.max()), float(raw.max())

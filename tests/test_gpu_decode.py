@@ -1,7 +1,8 @@
 """GPU parity of decode attention against the oracle's fp64 attention on the
-same dequantized K/V: per (sequence, q head) relative L2 error <= 2e-3 and
-elementwise abs error <= 1e-2 on the bf16 output (elements with |ref| >= 4,
-where no bf16 value is within 1e-2, compare against bf16(ref))."""
+same dequantized K/V.  Tolerance (per sequence and q head): relative L2 error
+<= 2e-3 and elementwise abs error <= 1e-2, both counted in excess of the
+exact answer's own bf16 rounding -- bf16(ref) is the best any bf16 output can
+be, and its rounding alone exceeds 2e-3 relative L2 on some vectors."""
 import numpy as np
 import pytest
 import torch
