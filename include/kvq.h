@@ -156,6 +156,31 @@ kvq_status kvq_decode_attention(kvq_cache* cache, int layer, const void* q_bf16,
 size_t kvq_decode_workspace_size(const kvq_cache* cache, int batch, int num_q_heads,
                                  int max_pages_per_seq);
 
+/* Size of the static scratch array of kvq_decode_attention_noalloc (16 MiB). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * kvq_decode_attention without a workspace argument, for callers that cannot
+ * allocate device memory when they decode: an application that must not call
+ * cudaMalloc/cudaFree after start-up (those calls may synchronize the device
+ * and can fail once memory is committed), or a plugin whose host framework
+ * owns all device memory and gives it no allocator.  The pages have no
+ * counterpart of this call; it is an addition of this library.
+ * Same arguments, semantics and errors as kvq_decode_attention, minus the
+ * workspace.  The split-K scratch is a file-scope static device array of
+ * KVQ_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps until the
+ * process exits; this call allocates nothing.  Sizes whose workspace
+ * (kvq_decode_workspace_size) exceeds that array are rejected with
+ * KVQ_ERR_UNSUPPORTED and a message.  The first call on a device resolves the
+ * array's device address (cudaGetSymbolAddress) with that device current, so
+ * make that first call before any stream capture.  All calls share the array:
+ * calls that overlap on the GPU (other streams or host threads) race.
+ */
+kvq_status kvq_decode_attention_noalloc(kvq_cache* cache, int layer, const void* q_bf16,
+                                        int num_q_heads, const int32_t* page_table,
+                                        int max_pages_per_seq, const int32_t* seq_lens, int batch,
+                                        float sm_scale, void* out_bf16, kvq_stream stream);
+
 /*
  * Gather and dequantize rows back to bf16 ([NVFP4] dequantize_prev_kv, here
  * to bf16 instead of an FP8 workspace; a test and debugging utility):

@@ -32,6 +32,7 @@ def _load():
         "kvq_quantize_and_store": ([vp, i32, vp, vp, vp, i32, vp, vp], i32),
         "kvq_decode_attention": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp, sz, vp], i32),
         "kvq_decode_workspace_size": ([vp, i32, i32, i32], sz),
+        "kvq_decode_attention_noalloc": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp], i32),
         "kvq_dequantize": ([vp, i32, vp, i32, vp, vp, vp], i32),
         "kvq_cache_layout": ([vp, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                               ctypes.POINTER(vp), ctypes.POINTER(sz)], i32),
@@ -134,6 +135,17 @@ def kvq_decode_attention(handle, layer, q, page_table, seq_lens, sm_scale, out, 
                                     _ptr(out), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "kvq_decode_attention")
+
+
+def kvq_decode_attention_noalloc(handle, layer, q, page_table, seq_lens, sm_scale, out,
+                                 stream=None):
+    """kvq_decode_attention with the library's static scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    B, Hq, _ = q.shape
+    _check(lib.kvq_decode_attention_noalloc(ctypes.c_void_p(handle), layer, _ptr(q), Hq,
+                                            _ptr(page_table), int(page_table.shape[1]),
+                                            _ptr(seq_lens), B, float(sm_scale), _ptr(out),
+                                            _stream(stream)), "kvq_decode_attention_noalloc")
 
 
 def kvq_dequantize(handle, layer, slot_mapping, k_out, v_out, stream=None):

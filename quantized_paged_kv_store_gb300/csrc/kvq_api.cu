@@ -83,6 +83,15 @@ bool uses_scales(kvq_format f) { return f == KVQ_FP8_E4M3 || f == KVQ_FP8_E5M2 |
 
 }  // namespace
 
+namespace kvq {
+void set_error_message(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+}
+}  // namespace kvq
+
 extern "C" {
 
 const char* kvq_last_error_string(void) { return g_msg; }

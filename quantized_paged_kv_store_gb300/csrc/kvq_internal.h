@@ -41,6 +41,9 @@ inline size_t data_row_bytes(kvq_format f, int head_dim) {
 }
 inline bool has_block_scales(kvq_format f) { return f == KVQ_FP4_BLOCK16 || f == KVQ_NVFP4; }
 
+// Sets the thread-local message returned by kvq_last_error_string().
+void set_error_message(const char* fmt, ...);
+
 // ---- launchers (defined in the .cu files; return a CUDA error code) -------
 
 cudaError_t launch_store(const Geometry& g, const LayerView& L, const void* k, const void* v,
