@@ -37,9 +37,11 @@ METRIC = "decode-attn KV GB/s and tokens/s at 32K ctx×32 seqs (fp8/fp4) vs HBM 
 FALLBACK_HBM_GBS = 6800.0   # one earlier GB300 copy-bandwidth measurement
 # Bytes per (token, kv head) of K plus V at head_dim 128.
 KV_BYTES = {"bf16": 512, "fp8_e4m3": 256, "fp8_e5m2": 256, "fp4_mx_block16": 144, "nvfp4": 144}
-DTYPE = {"bf16": "bf16 cache, f32 math", "fp8_e4m3": "e4m3 cache, f32 math",
-         "fp8_e5m2": "e5m2 cache, f32 math", "fp4_mx_block16": "e2m1+e8m0 cache, f32 math",
-         "nvfp4": "e2m1+e4m3 cache, f32 math"}
+DTYPE = {"bf16": "bf16 cache; bf16 mma, f32 accumulate",
+         "fp8_e4m3": "e4m3 cache; f16 mma, f32 accumulate",
+         "fp8_e5m2": "e5m2 cache; f16 mma, f32 accumulate",
+         "fp4_mx_block16": "e2m1+e8m0 cache; f16 mma, f32 accumulate",
+         "nvfp4": "e2m1+e4m3 cache; f16 mma, f32 accumulate"}
 # dram read+write bytes per decode-kernel launch from an ncu capture, keyed by
 # the hash of the decode sources it was taken on (stale hash -> null)
 NCU_TRAFFIC = {}
@@ -56,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--sweep", default=None, help="also run the format x context x batch sweep, "
                    "one JSON line per cell appended to this file")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--batch", type=int, default=32,
+                   help="sequences per rank (32 is the specified workload; smaller only for profiling)")
     return p.parse_args(argv)
 
 
@@ -196,7 +201,7 @@ def store_bytes(wl, fmt):
 def make_workload(fmt, seed, T=None, B=None):
     import synth
     if T is None:
-        wl = synth.cfg4_nvfp4_70b_32k(seed=seed)
+        wl = synth.cfg4_nvfp4_70b_32k(seed=seed, B=B or 32)
         if fmt != "nvfp4":
             wl.fmt = fmt
             wl.name = wl.name.replace("nvfp4", fmt)
@@ -234,7 +239,7 @@ def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True):
     rank, world, local = dist_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = make_workload(fmt, args.seed + 7919 * rank, T, B)
+    wl = make_workload(fmt, args.seed + 7919 * rank, T, B if T is not None else args.batch)
     ks, vs = wl.kv_all(0)
     scales = [float(x) for x in wl.scales(0)]
     cache = kvq.KVQCache(fmt, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
@@ -352,7 +357,7 @@ def run_ours(args):
     import torch
     rank, world = dist_init("nccl")
     fmt = args.format
-    r = run_cell(args, fmt, with_cpu=not args.no_cpu_baseline)
+    r = run_cell(args, fmt, with_cpu=not args.no_cpu_baseline, with_e2e=not args.no_e2e)
     wl = r["wl"]
     peak, peak_kind = peak_hbm()
     achieved = r["decode_bytes"] / (r["decode_ms"] * 1e-3) / 1e9

@@ -12,9 +12,32 @@
 //   all units' tiles are laid end to end (b-major) into one range of Wtot
 //   tiles, and warp worker w takes [w Wtot / NW, (w + 1) Wtot / NW).
 //   A worker emits one partial (o normalized, lse in log2 units) per unit it
-//   touches into slot u + w (unique, see plan_decode), and the merge kernel
-//   combines a unit's partials with the log-sum-exp rule
+//   touches into slot u + w (unique), and the merge kernel combines a unit's
+//   partials with the log-sum-exp rule
 //     out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s.
+//
+// Per warp worker: a private ring of shared-memory stages; lane 0 stages each
+// 16-token (page, kv head) tile of K, V (and their block scales) with 1D bulk
+// async copies (TMA engine) completing on an mbarrier, several tiles ahead.
+// Each tile then runs, with the lane layout of mma.m16n8k16 (lane = 4 r + q):
+//   QK^T on tensor cores: M = 16 tokens, N = 8 q heads of the group, K = d.
+//     The contraction index is permuted so that k-step j of thread q reads
+//     d = 32 q + 4 j + {0..3}: each thread's K operand is one contiguous
+//     byte run of its two token rows; Q is permuted the same way.
+//   online softmax per q head (base 2), P to f16, transposed with movmatrix
+//     into the B operand of
+//   PV on tensor cores: M = 16 head_dim rows (8 tiles), N = 8 q heads,
+//     K = 16 tokens.  Thread (r, q) owns head_dim block r (d = 16 r .. +15)
+//     of tokens {2q, 2q+1, 2q+8, 2q+9}: code pairs of two tokens are gathered
+//     with byte/nibble permutes and converted with cvt.f16x2.{e4m3x2, e5m2x2,
+//     e2m1x2}.
+// Exactness: E4M3/E5M2 codes and E2M1 x E4M3 products are exact in f16; Q
+// (bf16) is scaled by a power of two per head so it is exact in f16; FP4
+// block-16 values are held as E2M1 x 2^(E - E_ref) with E_ref the largest
+// exponent of the K row / the running largest of the V block, and the 2^E_ref
+// factor is applied in fp32.  The bf16 cache uses bf16 MMAs, with P split into
+// a high and a low bf16 part.  Per-tensor scales fold into the logit scale
+// (K) and the output (V).  Accumulation is fp32.
 #include "kvq_codecs.cuh"
 #include "kvq_internal.h"
 
@@ -27,6 +50,20 @@ constexpr int kWarpsPerCta = 4;
 constexpr int kHeadDim = 128;
 constexpr int kTile = 16;      // tokens per tile
 constexpr int kGroupMax = 8;   // q heads per unit
+constexpr int kPidWin = 32;    // page ids prefetched per window
+constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before giving up (~1 s)
+
+template <kvq_format F>
+struct Traits {
+  static constexpr int kRow = (F == KVQ_BF16) ? 256 : (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) ? 128 : 64;
+  static constexpr bool kScales = (F == KVQ_FP4_BLOCK16 || F == KVQ_NVFP4);
+  static constexpr int kData = kTile * kRow;          // one K (or V) tile
+  static constexpr int kScale = kScales ? kTile * 8 : 0;
+  static constexpr int kStage = 2 * (kData + kScale);
+  static constexpr int kStages = (F == KVQ_BF16) ? 3 : 4;
+  static constexpr int kWarpSmem = kStages * kStage;
+  static constexpr int kCtaSmem = kWarpsPerCta * (kWarpSmem + kStages * 8);
+};
 
 struct DecodeArgs {
   const uint16_t* q;
@@ -48,12 +85,80 @@ struct DecodeArgs {
   int* err;
 };
 
-__device__ __forceinline__ int warp_sum_i(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
-__device__ __forceinline__ float warp_sum_f(float v) {
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+
+__device__ __forceinline__ void mma_f16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_bf16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t r;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t f32x2_to_h2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t f32x2_to_bf2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Byte k (compile-time) of x: two E2M1 codes -> half2.
+template <int K>
+__device__ __forceinline__ uint32_t e2m1_byte_h2(uint32_t x) { return dec2_e2m1_h2<K>(x); }
+
+// f16 bits of 2^d for d <= 0 (exact down to 2^-24, 0 below).
+__device__ __forceinline__ uint32_t h_pow2_nonpos(int d) {
+  if (d >= -14) return (uint32_t)(d + 15) << 10;
+  if (d >= -24) return 1u << (d + 24);
+  return 0u;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
@@ -70,106 +175,490 @@ __device__ __forceinline__ long long worker_start(long long total, int w, int nw
   return total * w / nw;
 }
 
-// Four exact dequantized values of row `row` at head_dim indices 4*lane..+3
-// (without the per-tensor factor, which is folded into q or the output).
-template <kvq_format F>
-__device__ __forceinline__ void load4(const uint8_t* data, const uint8_t* scl, long long row,
-                                      int lane, float v[4]) {
-  if (F == KVQ_BF16) {
-    const uint2 w = *reinterpret_cast<const uint2*>(data + row * (kHeadDim * 2) + lane * 8);
-    v[0] = bf16_bits_to_float(w.x & 0xFFFF);
-    v[1] = bf16_bits_to_float(w.x >> 16);
-    v[2] = bf16_bits_to_float(w.y & 0xFFFF);
-    v[3] = bf16_bits_to_float(w.y >> 16);
-  } else if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(data + row * kHeadDim + lane * 4);
-    const uint32_t lo = (F == KVQ_FP8_E4M3) ? dec2_e4m3_h2(w) : dec2_e5m2_h2(w);
-    const uint32_t hi = (F == KVQ_FP8_E4M3) ? dec2_e4m3_h2_hi(w) : dec2_e5m2_h2_hi(w);
-    v[0] = h2_lo(lo);
-    v[1] = h2_hi(lo);
-    v[2] = h2_lo(hi);
-    v[3] = h2_hi(hi);
-  } else {
-    const uint32_t w = *reinterpret_cast<const uint16_t*>(data + row * (kHeadDim / 2) + lane * 2);
-    const uint32_t sc = scl[row * (kHeadDim / 16) + (lane >> 2)];
-    const float S = (F == KVQ_FP4_BLOCK16) ? dec_e8m0(sc) : dec_e4m3(sc);
-    const uint32_t h0 = dec2_e2m1_h2<0>(w), h1 = dec2_e2m1_h2<1>(w);
-    v[0] = h2_lo(h0) * S;
-    v[1] = h2_hi(h0) * S;
-    v[2] = h2_lo(h1) * S;
-    v[3] = h2_hi(h1) * S;
-  }
-}
+// Per-warp staging ring.
+struct Ring {
+  const uint8_t* gsmem;  // generic address of stage 0
+  uint32_t smem;         // shared address of stage 0
+  uint32_t bar;          // shared address of the first mbarrier
+  uint32_t pos;          // tiles consumed by this warp (monotonic)
+  uint32_t issued;       // tiles issued by this warp (monotonic)
+  uint32_t dead_pos;     // first tile whose wait ran out
+  bool dead;             // a wait ran out: issue and wait no more
+};
 
-// One worker's contribution to unit (b, h, hg) over tiles [t0, t1): simple
-// CUDA-core form, lane l owns head_dim indices 4l..4l+3.
+// One worker's contribution to unit (b, h, hg) over tiles [t0, t1).
 template <kvq_format F>
-__device__ void segment_simple(const DecodeArgs& a, int w, int b, int h, int hg, int t0, int t1) {
+__device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, int hg, int t0, int t1) {
+  using Tr = Traits<F>;
+  constexpr int S = Tr::kStages;
   const int lane = threadIdx.x & 31;
+  const int r = lane >> 2, q = lane & 3;
   const int T = __ldg(a.seq_lens + b);
   const int gh = min(kGroupMax, a.G - hg * kGroupMax);
-  float q[kGroupMax][4], m[kGroupMax], l[kGroupMax], o[kGroupMax][4];
+  const int n = t1 - t0;
+
+  // ---- Q fragments (B operand of QK^T) and per-head logit scales ----------
+  uint32_t qb[8][2];
+  float colscale;  // for head r, then redistributed
+  {
+    uint32_t w16[16];
+    if (r < gh) {
+      const uint16_t* qr = a.q + ((long long)b * a.Hq + h * a.G + hg * kGroupMax + r) * kHeadDim + q * 32;
 #pragma unroll
-  for (int g = 0; g < kGroupMax; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qr + i * 8);
+        w16[4 * i] = v.x;
+        w16[4 * i + 1] = v.y;
+        w16[4 * i + 2] = v.z;
+        w16[4 * i + 3] = v.w;
+      }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) { q[g][i] = 0.f; o[g][i] = 0.f; }
-    if (g < gh) {
-      const uint16_t* qr = a.q + ((long long)b * a.Hq + h * a.G + hg * kGroupMax + g) * kHeadDim;
-      const uint2 qw = *reinterpret_cast<const uint2*>(qr + lane * 4);
-      q[g][0] = bf16_bits_to_float(qw.x & 0xFFFF) * a.qscale;
-      q[g][1] = bf16_bits_to_float(qw.x >> 16) * a.qscale;
-      q[g][2] = bf16_bits_to_float(qw.y & 0xFFFF) * a.qscale;
-      q[g][3] = bf16_bits_to_float(qw.y >> 16) * a.qscale;
+      for (int i = 0; i < 16; ++i) w16[i] = 0u;
+    }
+    if (F == KVQ_BF16) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        qb[j][0] = w16[2 * j];
+        qb[j][1] = w16[2 * j + 1];
+      }
+      colscale = (r < gh) ? a.qscale : 0.f;
+    } else {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        amax = fmaxf(amax, fabsf(bf16_bits_to_float(w16[i] & 0xFFFF)));
+        amax = fmaxf(amax, fabsf(bf16_bits_to_float(w16[i] >> 16)));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      // power-of-two prescale: max |q'| in [2^14, 2^15) keeps bf16 values exact in f16
+      const int sq = amax > 0.f ? max(-126, min(126, floor_log2(amax) - 14)) : 0;
+      const float mul = exp2i(-sq);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        qb[j][0] = f32x2_to_h2(bf16_bits_to_float(w16[2 * j] & 0xFFFF) * mul,
+                               bf16_bits_to_float(w16[2 * j] >> 16) * mul);
+        qb[j][1] = f32x2_to_h2(bf16_bits_to_float(w16[2 * j + 1] & 0xFFFF) * mul,
+                               bf16_bits_to_float(w16[2 * j + 1] >> 16) * mul);
+      }
+      colscale = (r < gh) ? a.qscale * exp2i(sq) : 0.f;
     }
   }
+  // D1 columns of this thread are heads 2q, 2q+1 (held by lanes 8q and 8q+4 above)
+  const float cs0 = __shfl_sync(0xffffffffu, colscale, 8 * q);
+  const float cs1 = __shfl_sync(0xffffffffu, colscale, 8 * q + 4);
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  int vref = -1000;  // FP4 block-16: reference exponent code of V block r
   bool poison = false;
-  for (int t = t0; t < t1; ++t) {
-    const int tok0 = t * kTile;
-    const int page = __ldg(a.page_table + (long long)b * a.max_pages + tok0 / a.P);
-    if (page < 0 || page >= a.num_pages) { poison = true; continue; }
-    const long long row0 = ((long long)page * a.H + h) * a.P + tok0 % a.P;
-    const int ntok = min(kTile, T - tok0);
-    for (int j = 0; j < ntok; ++j) {
-      float kv[4];
-      load4<F>(a.kd, a.ks, row0 + j, lane, kv);
-      float z[kGroupMax];
-#pragma unroll
-      for (int g = 0; g < kGroupMax; ++g)
-        z[g] = warp_sum_f(q[g][0] * kv[0] + q[g][1] * kv[1] + q[g][2] * kv[2] + q[g][3] * kv[3]);
-      load4<F>(a.vd, a.vs, row0 + j, lane, kv);
-#pragma unroll
-      for (int g = 0; g < kGroupMax; ++g) {
-        const float mn = fmaxf(m[g], z[g]);
-        const float al = exp2f(m[g] - mn);
-        const float p = exp2f(z[g] - mn);
-        l[g] = l[g] * al + p;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[g][i] = o[g][i] * al + p * kv[i];
-        m[g] = mn;
+
+  // ---- page ids, prefetched one window ahead -------------------------------
+  const int tiles_per_page = a.P / kTile;
+  const int32_t* prow = a.page_table + (long long)b * a.max_pages;
+  auto load_pid = [&](int win) -> int {
+    const int t = t0 + win * kPidWin + lane;
+    return (t < t1) ? __ldg(prow + t / tiles_per_page) : -1;
+  };
+  int pid_cur = load_pid(0), pid_next = load_pid(1);
+  uint32_t bad_mask = 0;  // stages whose tile had an invalid page id (warp-uniform)
+
+  // issue tile k (relative) into stage issued % S; all lanes call
+  auto issue = [&](int k) {
+    if (k > 0 && (k % kPidWin) == 0) {
+      pid_cur = pid_next;
+      pid_next = load_pid(k / kPidWin + 1);
+    }
+    const int page = __shfl_sync(0xffffffffu, pid_cur, k % kPidWin);
+    const uint32_t st = ring.issued % S;
+    const uint32_t bar = ring.bar + 8 * st;
+    const bool ok = page >= 0 && page < a.num_pages;
+    bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
+    if (lane == 0) {
+      if (ok) {
+        const int tile = t0 + k;
+        const long long row0 =
+            ((long long)page * a.H + h) * a.P + (long long)(tile % tiles_per_page) * kTile;
+        const uint32_t dst = ring.smem + st * Tr::kStage;
+        mbar_arrive_tx(bar, Tr::kStage);
+        bulk_g2s(dst, a.kd + row0 * Tr::kRow, Tr::kData, bar);
+        bulk_g2s(dst + Tr::kData, a.vd + row0 * Tr::kRow, Tr::kData, bar);
+        if (Tr::kScales) {
+          bulk_g2s(dst + 2 * Tr::kData, a.ks + row0 * 8, Tr::kScale, bar);
+          bulk_g2s(dst + 2 * Tr::kData + Tr::kScale, a.vs + row0 * 8, Tr::kScale, bar);
+        }
+      } else {
+        mbar_arrive_tx(bar, 0);  // completes the phase without data
       }
     }
+    ring.issued++;
+  };
+
+  if (!ring.dead)
+    for (int k = 0; k < min(S, n); ++k) issue(k);
+
+  for (int i = 0; i < n; ++i) {
+    const uint32_t st = ring.pos % S;
+    const uint32_t parity = (ring.pos / S) & 1u;
+    if (!ring.dead) {
+      uint32_t polls = 0;
+      bool ok = mbar_try_wait(ring.bar + 8 * st, parity);
+      while (!ok && ++polls < kWaitLimit) ok = mbar_try_wait(ring.bar + 8 * st, parity);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        ring.dead = true;
+        ring.dead_pos = ring.pos;
+        if (lane == 0) atomicOr(a.err, kErrTimeout);
+      }
+    }
+    if (ring.dead || (bad_mask >> st) & 1u) {
+      poison = true;
+      ring.pos++;
+      continue;
+    }
+    const uint8_t* sbase = ring.gsmem + st * Tr::kStage;
+    const uint8_t* sK = sbase;
+    const uint8_t* sV = sbase + Tr::kData;
+    const uint8_t* sKs = sbase + 2 * Tr::kData;
+    const uint8_t* sVs = sKs + Tr::kScale;
+    const int tok0 = (t0 + i) * kTile;
+    const int nvalid = min(kTile, T - tok0);
+
+    // ---------------- S = Q K^T (tokens x heads) ----------------
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    float rs0 = 1.f, rs1 = 1.f;  // FP4 block-16 row scales 2^Emax
+    if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
+      const uint4 x0 = lds128(sK + r * 128 + q * 32), x1 = lds128(sK + r * 128 + q * 32 + 16);
+      const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
+      const uint32_t kr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t kr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t a0, a1, a2, a3;
+        if (F == KVQ_FP8_E4M3) {
+          a0 = dec2_e4m3_h2(kr[j]);
+          a2 = dec2_e4m3_h2_hi(kr[j]);
+          a1 = dec2_e4m3_h2(kr8[j]);
+          a3 = dec2_e4m3_h2_hi(kr8[j]);
+        } else {
+          a0 = dec2_e5m2_h2(kr[j]);
+          a2 = dec2_e5m2_h2_hi(kr[j]);
+          a1 = dec2_e5m2_h2(kr8[j]);
+          a3 = dec2_e5m2_h2_hi(kr8[j]);
+        }
+        mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+      }
+    } else if (F == KVQ_BF16) {
+      uint32_t kr[16], kr8[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 x = lds128(sK + r * 256 + q * 64 + 16 * c);
+        const uint4 y = lds128(sK + (r + 8) * 256 + q * 64 + 16 * c);
+        kr[4 * c] = x.x; kr[4 * c + 1] = x.y; kr[4 * c + 2] = x.z; kr[4 * c + 3] = x.w;
+        kr8[4 * c] = y.x; kr8[4 * c + 1] = y.y; kr8[4 * c + 2] = y.z; kr8[4 * c + 3] = y.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mma_bf16(s, kr[2 * j], kr8[2 * j], kr[2 * j + 1], kr8[2 * j + 1], qb[j][0], qb[j][1]);
+    } else {
+      const uint4 x = lds128(sK + r * 64 + q * 16);
+      const uint4 y = lds128(sK + (r + 8) * 64 + q * 16);
+      const uint32_t sc0 = *reinterpret_cast<const uint16_t*>(sKs + r * 8 + 2 * q);
+      const uint32_t sc1 = *reinterpret_cast<const uint16_t*>(sKs + (r + 8) * 8 + 2 * q);
+      uint32_t f00, f01, f10, f11;  // f16x2 factors: row r / r+8, block 2q / 2q+1
+      if (F == KVQ_NVFP4) {
+        const uint32_t h0 = dec2_e4m3_h2(sc0), h1 = dec2_e4m3_h2(sc1);
+        f00 = __byte_perm(h0, 0, 0x1010);
+        f01 = __byte_perm(h0, 0, 0x3232);
+        f10 = __byte_perm(h1, 0, 0x1010);
+        f11 = __byte_perm(h1, 0, 0x3232);
+      } else {
+        // row maximum exponent over the 8 blocks (4 lanes x 2 blocks)
+        int e0 = max((int)(sc0 & 0xFF), (int)(sc0 >> 8));
+        int e1 = max((int)(sc1 & 0xFF), (int)(sc1 >> 8));
+        e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 1));
+        e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 2));
+        e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 1));
+        e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 2));
+        f00 = h_pow2_nonpos((int)(sc0 & 0xFF) - e0) * 0x10001u;
+        f01 = h_pow2_nonpos((int)(sc0 >> 8) - e0) * 0x10001u;
+        f10 = h_pow2_nonpos((int)(sc1 & 0xFF) - e1) * 0x10001u;
+        f11 = h_pow2_nonpos((int)(sc1 >> 8) - e1) * 0x10001u;
+        rs0 = exp2i(e0 - 127);
+        rs1 = exp2i(e1 - 127);
+      }
+      const uint32_t kw[4] = {x.x, x.y, x.z, x.w}, kw8[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t wr = kw[j >> 1], wr8 = kw8[j >> 1];
+        uint32_t a0, a1, a2, a3;
+        if ((j & 1) == 0) {
+          a0 = e2m1_byte_h2<0>(wr);
+          a2 = e2m1_byte_h2<1>(wr);
+          a1 = e2m1_byte_h2<0>(wr8);
+          a3 = e2m1_byte_h2<1>(wr8);
+        } else {
+          a0 = e2m1_byte_h2<2>(wr);
+          a2 = e2m1_byte_h2<3>(wr);
+          a1 = e2m1_byte_h2<2>(wr8);
+          a3 = e2m1_byte_h2<3>(wr8);
+        }
+        const uint32_t fr = (j < 4) ? f00 : f01, fr8 = (j < 4) ? f10 : f11;
+        a0 = hmul2(a0, fr);
+        a2 = hmul2(a2, fr);
+        a1 = hmul2(a1, fr8);
+        a3 = hmul2(a3, fr8);
+        mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+      }
+    }
+
+    // ---------------- online softmax ----------------
+    s[0] *= cs0 * rs0;
+    s[1] *= cs1 * rs0;
+    s[2] *= cs0 * rs1;
+    s[3] *= cs1 * rs1;
+    if (r >= nvalid) s[0] = s[1] = -INFINITY;
+    if (r + 8 >= nvalid) s[2] = s[3] = -INFINITY;
+    float x0 = fmaxf(s[0], s[2]), x1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+    }
+    if (__any_sync(0xffffffffu, x0 > m0 || x1 > m1)) {
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+      l0 *= al0;
+      l1 *= al1;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+      m0 = n0;
+      m1 = n1;
+    }
+    const float p0 = exp2f(s[0] - m0), p1 = exp2f(s[1] - m1);
+    const float p2 = exp2f(s[2] - m0), p3 = exp2f(s[3] - m1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+
+    // ---------------- O^T += V^T P^T ----------------
+    const int ta = 2 * q, tb = 2 * q + 1, tc = 2 * q + 8, td = 2 * q + 9;
+    const bool partial = nvalid < kTile;
+    if (F == KVQ_BF16) {
+      const uint32_t ph0 = f32x2_to_bf2(p0, p1), ph1 = f32x2_to_bf2(p2, p3);
+      const float l0a = p0 - bf16_bits_to_float(ph0 & 0xFFFF), l1a = p1 - bf16_bits_to_float(ph0 >> 16);
+      const float l2a = p2 - bf16_bits_to_float(ph1 & 0xFFFF), l3a = p3 - bf16_bits_to_float(ph1 >> 16);
+      const uint32_t pl0 = f32x2_to_bf2(l0a, l1a), pl1 = f32x2_to_bf2(l2a, l3a);
+      const uint32_t bh0 = movm_t(ph0), bh1 = movm_t(ph1), bl0 = movm_t(pl0), bl1 = movm_t(pl1);
+      uint32_t va[8], vb[8], vc[8], vd[8];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint4 A = lds128(sV + ta * 256 + r * 32 + 16 * c), Bv = lds128(sV + tb * 256 + r * 32 + 16 * c);
+        const uint4 C = lds128(sV + tc * 256 + r * 32 + 16 * c), D = lds128(sV + td * 256 + r * 32 + 16 * c);
+        va[4 * c] = A.x; va[4 * c + 1] = A.y; va[4 * c + 2] = A.z; va[4 * c + 3] = A.w;
+        vb[4 * c] = Bv.x; vb[4 * c + 1] = Bv.y; vb[4 * c + 2] = Bv.z; vb[4 * c + 3] = Bv.w;
+        vc[4 * c] = C.x; vc[4 * c + 1] = C.y; vc[4 * c + 2] = C.z; vc[4 * c + 3] = C.w;
+        vd[4 * c] = D.x; vd[4 * c + 1] = D.y; vd[4 * c + 2] = D.z; vd[4 * c + 3] = D.w;
+      }
+      if (partial) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (ta >= nvalid) va[k] = 0u;
+          if (tb >= nvalid) vb[k] = 0u;
+          if (tc >= nvalid) vc[k] = 0u;
+          if (td >= nvalid) vd[k] = 0u;
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        // rows: d = 16 r + mt (word mt/2 of the block's first half), d = 16 r + 8 + mt
+        const uint32_t sel = (mt & 1) ? 0x7632u : 0x5410u;
+        const uint32_t a0 = __byte_perm(va[mt >> 1], vb[mt >> 1], sel);
+        const uint32_t a1 = __byte_perm(va[4 + (mt >> 1)], vb[4 + (mt >> 1)], sel);
+        const uint32_t a2 = __byte_perm(vc[mt >> 1], vd[mt >> 1], sel);
+        const uint32_t a3 = __byte_perm(vc[4 + (mt >> 1)], vd[4 + (mt >> 1)], sel);
+        mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+      }
+    } else {
+      const uint32_t b0 = movm_t(f32x2_to_h2(p0, p1)), b1 = movm_t(f32x2_to_h2(p2, p3));
+      if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
+        uint4 A = lds128(sV + ta * 128 + r * 16), Bv = lds128(sV + tb * 128 + r * 16);
+        uint4 C = lds128(sV + tc * 128 + r * 16), D = lds128(sV + td * 128 + r * 16);
+        if (partial) {
+          if (ta >= nvalid) A = make_uint4(0, 0, 0, 0);
+          if (tb >= nvalid) Bv = make_uint4(0, 0, 0, 0);
+          if (tc >= nvalid) C = make_uint4(0, 0, 0, 0);
+          if (td >= nvalid) D = make_uint4(0, 0, 0, 0);
+        }
+        const uint32_t aw[4] = {A.x, A.y, A.z, A.w}, bw[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
+        const uint32_t cw[4] = {C.x, C.y, C.z, C.w}, dw[4] = {D.x, D.y, D.z, D.w};
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          // byte mt (row r) and byte 8 + mt (row r + 8) of each token's block
+          const uint32_t sel = (mt & 2) ? 0x7362u : 0x5140u;
+          const uint32_t pab = __byte_perm(aw[mt >> 2], bw[mt >> 2], sel);
+          const uint32_t pab8 = __byte_perm(aw[2 + (mt >> 2)], bw[2 + (mt >> 2)], sel);
+          const uint32_t pcd = __byte_perm(cw[mt >> 2], dw[mt >> 2], sel);
+          const uint32_t pcd8 = __byte_perm(cw[2 + (mt >> 2)], dw[2 + (mt >> 2)], sel);
+          uint32_t a0, a1, a2, a3;
+          if (F == KVQ_FP8_E4M3) {
+            a0 = (mt & 1) ? dec2_e4m3_h2_hi(pab) : dec2_e4m3_h2(pab);
+            a1 = (mt & 1) ? dec2_e4m3_h2_hi(pab8) : dec2_e4m3_h2(pab8);
+            a2 = (mt & 1) ? dec2_e4m3_h2_hi(pcd) : dec2_e4m3_h2(pcd);
+            a3 = (mt & 1) ? dec2_e4m3_h2_hi(pcd8) : dec2_e4m3_h2(pcd8);
+          } else {
+            a0 = (mt & 1) ? dec2_e5m2_h2_hi(pab) : dec2_e5m2_h2(pab);
+            a1 = (mt & 1) ? dec2_e5m2_h2_hi(pab8) : dec2_e5m2_h2(pab8);
+            a2 = (mt & 1) ? dec2_e5m2_h2_hi(pcd) : dec2_e5m2_h2(pcd);
+            a3 = (mt & 1) ? dec2_e5m2_h2_hi(pcd8) : dec2_e5m2_h2(pcd8);
+          }
+          mma_f16(o[mt], a0, a1, a2, a3, b0, b1);
+        }
+      } else {
+        uint2 A = lds64(sV + ta * 64 + r * 8), Bv = lds64(sV + tb * 64 + r * 8);
+        uint2 C = lds64(sV + tc * 64 + r * 8), D = lds64(sV + td * 64 + r * 8);
+        if (partial) {
+          if (ta >= nvalid) A = make_uint2(0, 0);
+          if (tb >= nvalid) Bv = make_uint2(0, 0);
+          if (tc >= nvalid) C = make_uint2(0, 0);
+          if (td >= nvalid) D = make_uint2(0, 0);
+        }
+        uint32_t sa = sVs[ta * 8 + r], sb = sVs[tb * 8 + r];
+        uint32_t sc = sVs[tc * 8 + r], sd = sVs[td * 8 + r];
+        if (partial) {  // masked tokens: zero codes, and no say in the reference exponent
+          if (ta >= nvalid) sa = 0u;
+          if (tb >= nvalid) sb = 0u;
+          if (tc >= nvalid) sc = 0u;
+          if (td >= nvalid) sd = 0u;
+        }
+        uint32_t fab, fcd;  // f16x2 block factors (token pair)
+        if (F == KVQ_NVFP4) {
+          fab = dec2_e4m3_h2(sa | (sb << 8));
+          fcd = dec2_e4m3_h2(sc | (sd << 8));
+        } else {
+          // running reference exponent of V block r over the tokens seen
+          int et = max(max((int)sa, (int)sb), max((int)sc, (int)sd));
+          et = max(et, __shfl_xor_sync(0xffffffffu, et, 1));
+          et = max(et, __shfl_xor_sync(0xffffffffu, et, 2));
+          if (__any_sync(0xffffffffu, et > vref)) {
+            if (et > vref) {
+              const float f = (vref < -127) ? 0.f : exp2i(vref - et);
+#pragma unroll
+              for (int mt = 0; mt < 8; ++mt) {
+                o[mt][0] *= f;
+                o[mt][1] *= f;
+                o[mt][2] *= f;
+                o[mt][3] *= f;
+              }
+              vref = et;
+            }
+          }
+          fab = h_pow2_nonpos((int)sa - vref) | (h_pow2_nonpos((int)sb - vref) << 16);
+          fcd = h_pow2_nonpos((int)sc - vref) | (h_pow2_nonpos((int)sd - vref) << 16);
+        }
+        // nibble pairs (token a | token b << 4) for even / odd nibble index
+        const uint32_t ev0 = (A.x & 0x0F0F0F0Fu) | ((Bv.x << 4) & 0xF0F0F0F0u);
+        const uint32_t od0 = ((A.x >> 4) & 0x0F0F0F0Fu) | (Bv.x & 0xF0F0F0F0u);
+        const uint32_t ev1 = (A.y & 0x0F0F0F0Fu) | ((Bv.y << 4) & 0xF0F0F0F0u);
+        const uint32_t od1 = ((A.y >> 4) & 0x0F0F0F0Fu) | (Bv.y & 0xF0F0F0F0u);
+        const uint32_t ec0 = (C.x & 0x0F0F0F0Fu) | ((D.x << 4) & 0xF0F0F0F0u);
+        const uint32_t oc0 = ((C.x >> 4) & 0x0F0F0F0Fu) | (D.x & 0xF0F0F0F0u);
+        const uint32_t ec1 = (C.y & 0x0F0F0F0Fu) | ((D.y << 4) & 0xF0F0F0F0u);
+        const uint32_t oc1 = ((C.y >> 4) & 0x0F0F0F0Fu) | (D.y & 0xF0F0F0F0u);
+#define KVQ_PV_TILE(MT, ODD, BYTE)                                                       \
+  {                                                                                     \
+    const uint32_t a0 = hmul2(e2m1_byte_h2<BYTE>(ODD ? od0 : ev0), fab);                \
+    const uint32_t a1 = hmul2(e2m1_byte_h2<BYTE>(ODD ? od1 : ev1), fab);                \
+    const uint32_t a2 = hmul2(e2m1_byte_h2<BYTE>(ODD ? oc0 : ec0), fcd);                \
+    const uint32_t a3 = hmul2(e2m1_byte_h2<BYTE>(ODD ? oc1 : ec1), fcd);                \
+    mma_f16(o[MT], a0, a1, a2, a3, b0, b1);                                             \
   }
-  if (poison && lane == 0) atomicOr(a.err, kErrRange);
+        KVQ_PV_TILE(0, 0, 0)
+        KVQ_PV_TILE(1, 1, 0)
+        KVQ_PV_TILE(2, 0, 1)
+        KVQ_PV_TILE(3, 1, 1)
+        KVQ_PV_TILE(4, 0, 2)
+        KVQ_PV_TILE(5, 1, 2)
+        KVQ_PV_TILE(6, 0, 3)
+        KVQ_PV_TILE(7, 1, 3)
+#undef KVQ_PV_TILE
+      }
+    }
+
+    // release the stage and refill it with tile i + S
+    __syncwarp();
+    ring.pos++;
+    if (!ring.dead && i + S < n) {
+      if (lane == 0) fence_proxy_async();
+      issue(i + S);
+    }
+  }
+
+  // ---- partial result of this segment ----------------------------------------
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  poison = __any_sync(0xffffffffu, poison);
+  if (poison && lane == 0 && !ring.dead) atomicOr(a.err, kErrRange);
   const long long u = ((long long)b * a.H + h) * a.HG + hg;
   const long long slot = u + w;
-#pragma unroll
-  for (int g = 0; g < kGroupMax; ++g) {
-    if (g >= gh) break;
-    float* po = a.part_o + (slot * kGroupMax + g) * kHeadDim + lane * 4;
-    const float inv = poison ? 0.f : a.v_factor / l[g];
-    *reinterpret_cast<float4*>(po) = make_float4(o[g][0] * inv, o[g][1] * inv, o[g][2] * inv, o[g][3] * inv);
-    if (lane == 0) a.part_lse[slot * kGroupMax + g] = poison ? INFINITY : m[g] + __log2f(l[g]);
+  float vscale = a.v_factor;
+  if (F == KVQ_FP4_BLOCK16) vscale *= exp2i(max(-127, min(127, vref - 127)));
+  const float inv0 = poison ? 0.f : vscale / l0, inv1 = poison ? 0.f : vscale / l1;
+  // thread (r, q): heads 2q, 2q+1; d = 16 r + mt (c0, c1) and 16 r + 8 + mt (c2, c3)
+  if (2 * q < gh) {
+    float* po = a.part_o + (slot * kGroupMax + 2 * q) * kHeadDim + 16 * r;
+    reinterpret_cast<float4*>(po)[0] = make_float4(o[0][0] * inv0, o[1][0] * inv0, o[2][0] * inv0, o[3][0] * inv0);
+    reinterpret_cast<float4*>(po)[1] = make_float4(o[4][0] * inv0, o[5][0] * inv0, o[6][0] * inv0, o[7][0] * inv0);
+    reinterpret_cast<float4*>(po)[2] = make_float4(o[0][2] * inv0, o[1][2] * inv0, o[2][2] * inv0, o[3][2] * inv0);
+    reinterpret_cast<float4*>(po)[3] = make_float4(o[4][2] * inv0, o[5][2] * inv0, o[6][2] * inv0, o[7][2] * inv0);
+    if (r == 0) a.part_lse[slot * kGroupMax + 2 * q] = poison ? INFINITY : m0 + __log2f(l0);
+  }
+  if (2 * q + 1 < gh) {
+    float* po = a.part_o + (slot * kGroupMax + 2 * q + 1) * kHeadDim + 16 * r;
+    reinterpret_cast<float4*>(po)[0] = make_float4(o[0][1] * inv1, o[1][1] * inv1, o[2][1] * inv1, o[3][1] * inv1);
+    reinterpret_cast<float4*>(po)[1] = make_float4(o[4][1] * inv1, o[5][1] * inv1, o[6][1] * inv1, o[7][1] * inv1);
+    reinterpret_cast<float4*>(po)[2] = make_float4(o[0][3] * inv1, o[1][3] * inv1, o[2][3] * inv1, o[3][3] * inv1);
+    reinterpret_cast<float4*>(po)[3] = make_float4(o[4][3] * inv1, o[5][3] * inv1, o[6][3] * inv1, o[7][3] * inv1);
+    if (r == 0) a.part_lse[slot * kGroupMax + 2 * q + 1] = poison ? INFINITY : m1 + __log2f(l1);
   }
 }
 
 template <kvq_format F>
-__global__ void __launch_bounds__(kWarpsPerCta * 32) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs a) {
+  using Tr = Traits<F>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
   const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int warp = threadIdx.x >> 5;
+  const int w = blockIdx.x * kWarpsPerCta + warp;
+  // let the merge kernel launch early; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;");
   if (w >= a.num_workers) return;
   const long long upb = (long long)a.H * a.HG;  // units per sequence
+
+  Ring ring;
+  ring.gsmem = smem_raw + warp * Tr::kWarpSmem;
+  ring.smem = smem_addr(smem_raw) + warp * Tr::kWarpSmem;
+  ring.dead_pos = 0;
+  ring.bar = smem_addr(smem_raw) + kWarpsPerCta * Tr::kWarpSmem + warp * Tr::kStages * 8;
+  ring.pos = 0;
+  ring.issued = 0;
+  ring.dead = false;
+  if (lane == 0) {
+    for (int s = 0; s < Tr::kStages; ++s) mbar_init(ring.bar + 8 * s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async();
+  }
+  __syncwarp();
 
   // pass 1: total tiles; worker 0 reports invalid lengths and publishes Wtot
   long long total = 0;
@@ -198,7 +687,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) decode_kernel(DecodeArgs a)
   int b = 0;
   for (int b0 = 0; b0 < a.B; b0 += 32) {
     const int bb = b0 + lane;
-    long long x = (bb < a.B) ? (long long)tiles_of(a, bb) * upb : 0;
+    const long long x = (bb < a.B) ? (long long)tiles_of(a, bb) * upb : 0;
     long long incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -217,13 +706,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) decode_kernel(DecodeArgs a)
     cum += chunk;
   }
   int nt = tiles_of(a, b);
-  long long local = start - cum;
+  const long long local = start - cum;
   int ub = (int)(local / nt);
   int tile = (int)(local - (long long)ub * nt);
   long long pos = start;
   while (pos < end) {
     const int n = (int)min((long long)(nt - tile), end - pos);
-    segment_simple<F>(a, w, b, ub / a.HG, ub % a.HG, tile, tile + n);
+    segment<F>(a, ring, w, b, ub / a.HG, ub % a.HG, tile, tile + n);
     pos += n;
     tile += n;
     if (tile == nt) {
@@ -234,10 +723,21 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) decode_kernel(DecodeArgs a)
       }
     }
   }
+  // Every issued tile has been consumed, unless a wait ran out: then give the
+  // copies still in flight a bounded chance to land before the CTA exits.
+  if (ring.dead) {
+    for (uint32_t t = ring.dead_pos; t < ring.issued; ++t) {
+      const uint32_t bar = ring.bar + 8 * (t % Tr::kStages);
+      uint32_t polls = 0;
+      while (!mbar_try_wait(bar, (t / Tr::kStages) & 1u) && ++polls < kWaitLimit) {
+      }
+    }
+  }
 }
 
 // One CTA per sequence: combine each (unit, head)'s partials.
 __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ long long s_red[8];
@@ -302,6 +802,40 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+template <kvq_format F>
+cudaError_t prepare(int* ctas_per_sm) {
+  static int cached = 0;
+  if (!cached) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Traits<F>::kCtaSmem);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<F>, kWarpsPerCta * 32,
+                                                      Traits<F>::kCtaSmem);
+    if (e != cudaSuccess) return e;
+    cached = std::max(n, 1);
+  }
+  *ctas_per_sm = cached;
+  return cudaSuccess;
+}
+
+cudaError_t ctas_per_sm(kvq_format f, int* n) {
+  switch (f) {
+    case KVQ_BF16: return prepare<KVQ_BF16>(n);
+    case KVQ_FP8_E4M3: return prepare<KVQ_FP8_E4M3>(n);
+    case KVQ_FP8_E5M2: return prepare<KVQ_FP8_E5M2>(n);
+    case KVQ_FP4_BLOCK16: return prepare<KVQ_FP4_BLOCK16>(n);
+    case KVQ_NVFP4: return prepare<KVQ_NVFP4>(n);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <kvq_format F>
+cudaError_t launch_f(const DecodeArgs& a, int ctas, cudaStream_t stream) {
+  decode_kernel<F><<<ctas, kWarpsPerCta * 32, Traits<F>::kCtaSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_per_seq,
@@ -311,9 +845,13 @@ bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_pe
   if (num_q_heads % g.kv_heads != 0) { *why = "num_q_heads must be a multiple of kv_heads"; return false; }
   const int G = num_q_heads / g.kv_heads;
   if (G > 2 * kGroupMax) { *why = "group size num_q_heads / kv_heads must be <= 16"; return false; }
-  int sms = 0;
+  int sms = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0) {
     *why = "cannot query the SM count";
+    return false;
+  }
+  if (ctas_per_sm(g.fmt, &per_sm) != cudaSuccess) {
+    *why = "cannot configure the decode kernel";
     return false;
   }
   plan->group = G;
@@ -321,8 +859,9 @@ bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_pe
   plan->num_units = (int64_t)batch * g.kv_heads * plan->head_groups;
   const int64_t tiles_per_seq = ((int64_t)max_pages_per_seq * g.page_size + kTile - 1) / kTile;
   const int64_t max_tiles = std::max<int64_t>(1, plan->num_units * tiles_per_seq);
-  int64_t ctas = (int64_t)sms * 4;
-  ctas = std::min<int64_t>(ctas, (max_tiles + kWarpsPerCta - 1) / kWarpsPerCta);
+  // persistent grid: every resident warp is a worker, each with >= 4 tiles
+  int64_t ctas = (int64_t)sms * per_sm;
+  ctas = std::min<int64_t>(ctas, (max_tiles + 4 * kWarpsPerCta - 1) / (4 * kWarpsPerCta));
   ctas = std::max<int64_t>(ctas, 1);
   plan->ctas = (int)ctas;
   plan->num_workers = plan->ctas * kWarpsPerCta;
@@ -365,17 +904,27 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
   a.v_factor = v_factor;
   a.err = err;
   if (batch == 0) return cudaSuccess;
+  cudaError_t e = cudaErrorInvalidValue;
   switch (g.fmt) {
-    case KVQ_BF16: decode_kernel<KVQ_BF16><<<plan.ctas, kWarpsPerCta * 32, 0, stream>>>(a); break;
-    case KVQ_FP8_E4M3: decode_kernel<KVQ_FP8_E4M3><<<plan.ctas, kWarpsPerCta * 32, 0, stream>>>(a); break;
-    case KVQ_FP8_E5M2: decode_kernel<KVQ_FP8_E5M2><<<plan.ctas, kWarpsPerCta * 32, 0, stream>>>(a); break;
-    case KVQ_FP4_BLOCK16: decode_kernel<KVQ_FP4_BLOCK16><<<plan.ctas, kWarpsPerCta * 32, 0, stream>>>(a); break;
-    case KVQ_NVFP4: decode_kernel<KVQ_NVFP4><<<plan.ctas, kWarpsPerCta * 32, 0, stream>>>(a); break;
+    case KVQ_BF16: e = launch_f<KVQ_BF16>(a, plan.ctas, stream); break;
+    case KVQ_FP8_E4M3: e = launch_f<KVQ_FP8_E4M3>(a, plan.ctas, stream); break;
+    case KVQ_FP8_E5M2: e = launch_f<KVQ_FP8_E5M2>(a, plan.ctas, stream); break;
+    case KVQ_FP4_BLOCK16: e = launch_f<KVQ_FP4_BLOCK16>(a, plan.ctas, stream); break;
+    case KVQ_NVFP4: e = launch_f<KVQ_NVFP4>(a, plan.ctas, stream); break;
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  merge_kernel<<<batch, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  // merge: programmatic dependent launch (starts while the split kernel drains)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel, a);
 }
 
 }  // namespace kvq
