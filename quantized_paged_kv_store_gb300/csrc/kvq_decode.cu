@@ -57,10 +57,13 @@ template <kvq_format F>
 struct Traits {
   static constexpr int kRow = (F == KVQ_BF16) ? 256 : (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) ? 128 : 64;
   static constexpr bool kScales = (F == KVQ_FP4_BLOCK16 || F == KVQ_NVFP4);
-  static constexpr int kData = kTile * kRow;          // one K (or V) tile
-  static constexpr int kScale = kScales ? kTile * 8 : 0;
-  static constexpr int kStage = 2 * (kData + kScale);
-  static constexpr int kStages = (F == KVQ_BF16) ? 3 : 4;
+  static constexpr int kData = kTile * kRow;              // one K (or V) tile
+  static constexpr int kScale = kScales ? kTile * 8 : 0;  // its block scales
+  static constexpr int kTileBytes = 2 * (kData + kScale); // K, V (+ scales) of one tile
+  static constexpr int kCopies = kScales ? 4 : 2;         // bulk copies per tile
+  static constexpr int kTps = (F == KVQ_BF16) ? 1 : 2;    // tiles per stage
+  static constexpr int kStage = kTps * kTileBytes;
+  static constexpr int kStages = (F == KVQ_BF16) ? 3 : 2;
   static constexpr int kWarpSmem = kStages * kStage;
   static constexpr int kCtaSmem = kWarpsPerCta * (kWarpSmem + kStages * 8);
 };
@@ -77,6 +80,7 @@ struct DecodeArgs {
   float* part_o;      // [slots][8][128]
   float* part_lse;    // [slots][8]
   long long* meta;    // [0] = Wtot
+  long long* prefix;  // [B + 1]: tiles of sequences before b (written by worker 0)
   int B, H, Hq, G, HG, max_pages, P;
   long long num_pages;
   int num_workers;
@@ -151,6 +155,14 @@ __device__ __forceinline__ uint32_t f32x2_to_bf2(float lo, float hi) {
 template <int K>
 __device__ __forceinline__ uint32_t e2m1_byte_h2(uint32_t x) { return dec2_e2m1_h2<K>(x); }
 
+// 2^x by the hardware approximation; results below 2^-126 flush to zero,
+// which is harmless for softmax weights that small.
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // f16 bits of 2^d for d <= 0 (exact down to 2^-24, 0 below).
 __device__ __forceinline__ uint32_t h_pow2_nonpos(int d) {
   if (d >= -14) return (uint32_t)(d + 15) << 10;
@@ -180,22 +192,270 @@ struct Ring {
   const uint8_t* gsmem;  // generic address of stage 0
   uint32_t smem;         // shared address of stage 0
   uint32_t bar;          // shared address of the first mbarrier
-  uint32_t pos;          // tiles consumed by this warp (monotonic)
-  uint32_t issued;       // tiles issued by this warp (monotonic)
-  uint32_t dead_pos;     // first tile whose wait ran out
+  uint32_t pos;          // stages consumed by this warp (monotonic)
+  uint32_t issued;       // stages issued by this warp (monotonic)
+  uint32_t dead_pos;     // first stage whose wait ran out
   bool dead;             // a wait ran out: issue and wait no more
 };
+
+// Logits of one 16-token tile: s = (K^ Q'^T) for rows r, r+8 and heads 2q,
+// 2q+1 (before the per-head scale); rs0/rs1 are the FP4 block-16 row factors.
+template <kvq_format F>
+__device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, int r, int q,
+                                        const uint32_t (&qb)[8][2], float (&s)[4], float& rs0,
+                                        float& rs1) {
+  s[0] = s[1] = s[2] = s[3] = 0.f;
+  rs0 = rs1 = 1.f;
+  if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
+    const uint4 x0 = lds128(sK + r * 128 + q * 32), x1 = lds128(sK + r * 128 + q * 32 + 16);
+    const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
+    const uint32_t kr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const uint32_t kr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t a0, a1, a2, a3;
+      if (F == KVQ_FP8_E4M3) {
+        a0 = dec2_e4m3_h2(kr[j]);
+        a2 = dec2_e4m3_h2_hi(kr[j]);
+        a1 = dec2_e4m3_h2(kr8[j]);
+        a3 = dec2_e4m3_h2_hi(kr8[j]);
+      } else {
+        a0 = dec2_e5m2_h2(kr[j]);
+        a2 = dec2_e5m2_h2_hi(kr[j]);
+        a1 = dec2_e5m2_h2(kr8[j]);
+        a3 = dec2_e5m2_h2_hi(kr8[j]);
+      }
+      mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+    }
+  } else if (F == KVQ_BF16) {
+    uint32_t kr[16], kr8[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 x = lds128(sK + r * 256 + q * 64 + 16 * c);
+      const uint4 y = lds128(sK + (r + 8) * 256 + q * 64 + 16 * c);
+      kr[4 * c] = x.x; kr[4 * c + 1] = x.y; kr[4 * c + 2] = x.z; kr[4 * c + 3] = x.w;
+      kr8[4 * c] = y.x; kr8[4 * c + 1] = y.y; kr8[4 * c + 2] = y.z; kr8[4 * c + 3] = y.w;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mma_bf16(s, kr[2 * j], kr8[2 * j], kr[2 * j + 1], kr8[2 * j + 1], qb[j][0], qb[j][1]);
+  } else {
+    const uint4 x = lds128(sK + r * 64 + q * 16);
+    const uint4 y = lds128(sK + (r + 8) * 64 + q * 16);
+    const uint32_t sc0 = *reinterpret_cast<const uint16_t*>(sKs + r * 8 + 2 * q);
+    const uint32_t sc1 = *reinterpret_cast<const uint16_t*>(sKs + (r + 8) * 8 + 2 * q);
+    uint32_t f00, f01, f10, f11;  // f16x2 factors: row r / r+8, block 2q / 2q+1
+    if (F == KVQ_NVFP4) {
+      const uint32_t h0 = dec2_e4m3_h2(sc0), h1 = dec2_e4m3_h2(sc1);
+      f00 = __byte_perm(h0, 0, 0x1010);
+      f01 = __byte_perm(h0, 0, 0x3232);
+      f10 = __byte_perm(h1, 0, 0x1010);
+      f11 = __byte_perm(h1, 0, 0x3232);
+    } else {
+      // row maximum exponent over the 8 blocks (4 lanes x 2 blocks)
+      int e0 = max((int)(sc0 & 0xFF), (int)(sc0 >> 8));
+      int e1 = max((int)(sc1 & 0xFF), (int)(sc1 >> 8));
+      e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 1));
+      e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 2));
+      e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 1));
+      e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 2));
+      f00 = h_pow2_nonpos((int)(sc0 & 0xFF) - e0) * 0x10001u;
+      f01 = h_pow2_nonpos((int)(sc0 >> 8) - e0) * 0x10001u;
+      f10 = h_pow2_nonpos((int)(sc1 & 0xFF) - e1) * 0x10001u;
+      f11 = h_pow2_nonpos((int)(sc1 >> 8) - e1) * 0x10001u;
+      rs0 = exp2i(e0 - 127);
+      rs1 = exp2i(e1 - 127);
+    }
+    const uint32_t kw[4] = {x.x, x.y, x.z, x.w}, kw8[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t wr = kw[j >> 1], wr8 = kw8[j >> 1];
+      uint32_t a0, a1, a2, a3;
+      if ((j & 1) == 0) {
+        a0 = e2m1_byte_h2<0>(wr);
+        a2 = e2m1_byte_h2<1>(wr);
+        a1 = e2m1_byte_h2<0>(wr8);
+        a3 = e2m1_byte_h2<1>(wr8);
+      } else {
+        a0 = e2m1_byte_h2<2>(wr);
+        a2 = e2m1_byte_h2<3>(wr);
+        a1 = e2m1_byte_h2<2>(wr8);
+        a3 = e2m1_byte_h2<3>(wr8);
+      }
+      const uint32_t fr = (j < 4) ? f00 : f01, fr8 = (j < 4) ? f10 : f11;
+      a0 = hmul2(a0, fr);
+      a2 = hmul2(a2, fr);
+      a1 = hmul2(a1, fr8);
+      a3 = hmul2(a3, fr8);
+      mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+    }
+  }
+
+}
+
+// O^T += V^T P^T for one 16-token tile (p* are this thread's P entries:
+// rows r, r+8 and heads 2q, 2q+1); nvalid tokens of the tile are real.
+template <kvq_format F>
+__device__ __forceinline__ void tile_pv(const uint8_t* sV, const uint8_t* sVs, int r, int q, int nvalid,
+                                        float p0, float p1, float p2, float p3, float (&o)[8][4],
+                                        int& vref) {
+  const bool partial = nvalid < kTile;
+  const int ta = 2 * q, tb = 2 * q + 1, tc = 2 * q + 8, td = 2 * q + 9;
+  if (F == KVQ_BF16) {
+    const uint32_t ph0 = f32x2_to_bf2(p0, p1), ph1 = f32x2_to_bf2(p2, p3);
+    const float l0a = p0 - bf16_bits_to_float(ph0 & 0xFFFF), l1a = p1 - bf16_bits_to_float(ph0 >> 16);
+    const float l2a = p2 - bf16_bits_to_float(ph1 & 0xFFFF), l3a = p3 - bf16_bits_to_float(ph1 >> 16);
+    const uint32_t pl0 = f32x2_to_bf2(l0a, l1a), pl1 = f32x2_to_bf2(l2a, l3a);
+    const uint32_t bh0 = movm_t(ph0), bh1 = movm_t(ph1), bl0 = movm_t(pl0), bl1 = movm_t(pl1);
+    uint32_t va[8], vb[8], vc[8], vd[8];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint4 A = lds128(sV + ta * 256 + r * 32 + 16 * c), Bv = lds128(sV + tb * 256 + r * 32 + 16 * c);
+      const uint4 C = lds128(sV + tc * 256 + r * 32 + 16 * c), D = lds128(sV + td * 256 + r * 32 + 16 * c);
+      va[4 * c] = A.x; va[4 * c + 1] = A.y; va[4 * c + 2] = A.z; va[4 * c + 3] = A.w;
+      vb[4 * c] = Bv.x; vb[4 * c + 1] = Bv.y; vb[4 * c + 2] = Bv.z; vb[4 * c + 3] = Bv.w;
+      vc[4 * c] = C.x; vc[4 * c + 1] = C.y; vc[4 * c + 2] = C.z; vc[4 * c + 3] = C.w;
+      vd[4 * c] = D.x; vd[4 * c + 1] = D.y; vd[4 * c + 2] = D.z; vd[4 * c + 3] = D.w;
+    }
+    if (partial) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (ta >= nvalid) va[k] = 0u;
+        if (tb >= nvalid) vb[k] = 0u;
+        if (tc >= nvalid) vc[k] = 0u;
+        if (td >= nvalid) vd[k] = 0u;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      // rows: d = 16 r + mt (word mt/2 of the block's first half), d = 16 r + 8 + mt
+      const uint32_t sel = (mt & 1) ? 0x7632u : 0x5410u;
+      const uint32_t a0 = __byte_perm(va[mt >> 1], vb[mt >> 1], sel);
+      const uint32_t a1 = __byte_perm(va[4 + (mt >> 1)], vb[4 + (mt >> 1)], sel);
+      const uint32_t a2 = __byte_perm(vc[mt >> 1], vd[mt >> 1], sel);
+      const uint32_t a3 = __byte_perm(vc[4 + (mt >> 1)], vd[4 + (mt >> 1)], sel);
+      mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+      mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+    }
+  } else {
+    const uint32_t b0 = movm_t(f32x2_to_h2(p0, p1)), b1 = movm_t(f32x2_to_h2(p2, p3));
+    if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
+      uint4 A = lds128(sV + ta * 128 + r * 16), Bv = lds128(sV + tb * 128 + r * 16);
+      uint4 C = lds128(sV + tc * 128 + r * 16), D = lds128(sV + td * 128 + r * 16);
+      if (partial) {
+        if (ta >= nvalid) A = make_uint4(0, 0, 0, 0);
+        if (tb >= nvalid) Bv = make_uint4(0, 0, 0, 0);
+        if (tc >= nvalid) C = make_uint4(0, 0, 0, 0);
+        if (td >= nvalid) D = make_uint4(0, 0, 0, 0);
+      }
+      const uint32_t aw[4] = {A.x, A.y, A.z, A.w}, bw[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
+      const uint32_t cw[4] = {C.x, C.y, C.z, C.w}, dw[4] = {D.x, D.y, D.z, D.w};
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        // byte mt (row r) and byte 8 + mt (row r + 8) of each token's block
+        const uint32_t sel = (mt & 2) ? 0x7362u : 0x5140u;
+        const uint32_t pab = __byte_perm(aw[mt >> 2], bw[mt >> 2], sel);
+        const uint32_t pab8 = __byte_perm(aw[2 + (mt >> 2)], bw[2 + (mt >> 2)], sel);
+        const uint32_t pcd = __byte_perm(cw[mt >> 2], dw[mt >> 2], sel);
+        const uint32_t pcd8 = __byte_perm(cw[2 + (mt >> 2)], dw[2 + (mt >> 2)], sel);
+        uint32_t a0, a1, a2, a3;
+        if (F == KVQ_FP8_E4M3) {
+          a0 = (mt & 1) ? dec2_e4m3_h2_hi(pab) : dec2_e4m3_h2(pab);
+          a1 = (mt & 1) ? dec2_e4m3_h2_hi(pab8) : dec2_e4m3_h2(pab8);
+          a2 = (mt & 1) ? dec2_e4m3_h2_hi(pcd) : dec2_e4m3_h2(pcd);
+          a3 = (mt & 1) ? dec2_e4m3_h2_hi(pcd8) : dec2_e4m3_h2(pcd8);
+        } else {
+          a0 = (mt & 1) ? dec2_e5m2_h2_hi(pab) : dec2_e5m2_h2(pab);
+          a1 = (mt & 1) ? dec2_e5m2_h2_hi(pab8) : dec2_e5m2_h2(pab8);
+          a2 = (mt & 1) ? dec2_e5m2_h2_hi(pcd) : dec2_e5m2_h2(pcd);
+          a3 = (mt & 1) ? dec2_e5m2_h2_hi(pcd8) : dec2_e5m2_h2(pcd8);
+        }
+        mma_f16(o[mt], a0, a1, a2, a3, b0, b1);
+      }
+    } else {
+      uint2 A = lds64(sV + ta * 64 + r * 8), Bv = lds64(sV + tb * 64 + r * 8);
+      uint2 C = lds64(sV + tc * 64 + r * 8), D = lds64(sV + td * 64 + r * 8);
+      if (partial) {
+        if (ta >= nvalid) A = make_uint2(0, 0);
+        if (tb >= nvalid) Bv = make_uint2(0, 0);
+        if (tc >= nvalid) C = make_uint2(0, 0);
+        if (td >= nvalid) D = make_uint2(0, 0);
+      }
+      uint32_t sa = sVs[ta * 8 + r], sb = sVs[tb * 8 + r];
+      uint32_t sc = sVs[tc * 8 + r], sd = sVs[td * 8 + r];
+      if (partial) {  // masked tokens: zero codes, and no say in the reference exponent
+        if (ta >= nvalid) sa = 0u;
+        if (tb >= nvalid) sb = 0u;
+        if (tc >= nvalid) sc = 0u;
+        if (td >= nvalid) sd = 0u;
+      }
+      uint32_t fab, fcd;  // f16x2 block factors (token pair)
+      if (F == KVQ_NVFP4) {
+        fab = dec2_e4m3_h2(sa | (sb << 8));
+        fcd = dec2_e4m3_h2(sc | (sd << 8));
+      } else {
+        // running reference exponent of V block r over the tokens seen
+        int et = max(max((int)sa, (int)sb), max((int)sc, (int)sd));
+        et = max(et, __shfl_xor_sync(0xffffffffu, et, 1));
+        et = max(et, __shfl_xor_sync(0xffffffffu, et, 2));
+        if (__any_sync(0xffffffffu, et > vref)) {
+          if (et > vref) {
+            const float f = (vref < -127) ? 0.f : exp2i(vref - et);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              o[mt][0] *= f;
+              o[mt][1] *= f;
+              o[mt][2] *= f;
+              o[mt][3] *= f;
+            }
+            vref = et;
+          }
+        }
+        fab = h_pow2_nonpos((int)sa - vref) | (h_pow2_nonpos((int)sb - vref) << 16);
+        fcd = h_pow2_nonpos((int)sc - vref) | (h_pow2_nonpos((int)sd - vref) << 16);
+      }
+      // nibble pairs (token a | token b << 4) for even / odd nibble index
+      const uint32_t ev0 = (A.x & 0x0F0F0F0Fu) | ((Bv.x << 4) & 0xF0F0F0F0u);
+      const uint32_t od0 = ((A.x >> 4) & 0x0F0F0F0Fu) | (Bv.x & 0xF0F0F0F0u);
+      const uint32_t ev1 = (A.y & 0x0F0F0F0Fu) | ((Bv.y << 4) & 0xF0F0F0F0u);
+      const uint32_t od1 = ((A.y >> 4) & 0x0F0F0F0Fu) | (Bv.y & 0xF0F0F0F0u);
+      const uint32_t ec0 = (C.x & 0x0F0F0F0Fu) | ((D.x << 4) & 0xF0F0F0F0u);
+      const uint32_t oc0 = ((C.x >> 4) & 0x0F0F0F0Fu) | (D.x & 0xF0F0F0F0u);
+      const uint32_t ec1 = (C.y & 0x0F0F0F0Fu) | ((D.y << 4) & 0xF0F0F0F0u);
+      const uint32_t oc1 = ((C.y >> 4) & 0x0F0F0F0Fu) | (D.y & 0xF0F0F0F0u);
+#define KVQ_PV_TILE(MT, ODD, BYTE)                                                       \
+{                                                                                     \
+  const uint32_t a0 = hmul2(e2m1_byte_h2<BYTE>(ODD ? od0 : ev0), fab);                \
+  const uint32_t a1 = hmul2(e2m1_byte_h2<BYTE>(ODD ? od1 : ev1), fab);                \
+  const uint32_t a2 = hmul2(e2m1_byte_h2<BYTE>(ODD ? oc0 : ec0), fcd);                \
+  const uint32_t a3 = hmul2(e2m1_byte_h2<BYTE>(ODD ? oc1 : ec1), fcd);                \
+  mma_f16(o[MT], a0, a1, a2, a3, b0, b1);                                             \
+}
+      KVQ_PV_TILE(0, 0, 0)
+      KVQ_PV_TILE(1, 1, 0)
+      KVQ_PV_TILE(2, 0, 1)
+      KVQ_PV_TILE(3, 1, 1)
+      KVQ_PV_TILE(4, 0, 2)
+      KVQ_PV_TILE(5, 1, 2)
+      KVQ_PV_TILE(6, 0, 3)
+      KVQ_PV_TILE(7, 1, 3)
+#undef KVQ_PV_TILE
+    }
+  }
+
+}
 
 // One worker's contribution to unit (b, h, hg) over tiles [t0, t1).
 template <kvq_format F>
 __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, int hg, int t0, int t1) {
   using Tr = Traits<F>;
-  constexpr int S = Tr::kStages;
+  constexpr int S = Tr::kStages, TPS = Tr::kTps;
+  constexpr float kLazy = 8.f;  // rescale only when a logit beats the max by 2^8
   const int lane = threadIdx.x & 31;
   const int r = lane >> 2, q = lane & 3;
   const int T = __ldg(a.seq_lens + b);
   const int gh = min(kGroupMax, a.G - hg * kGroupMax);
   const int n = t1 - t0;
+  const int nch = (n + TPS - 1) / TPS;
 
   // ---- Q fragments (B operand of QK^T) and per-head logit scales ----------
   uint32_t qb[8][2];
@@ -256,7 +516,7 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
   int vref = -1000;  // FP4 block-16: reference exponent code of V block r
   bool poison = false;
 
-  // ---- page ids, prefetched one window ahead -------------------------------
+  // ---- page ids, prefetched one window (32 tiles) ahead ----------------------
   const int tiles_per_page = a.P / kTile;
   const int32_t* prow = a.page_table + (long long)b * a.max_pages;
   auto load_pid = [&](int win) -> int {
@@ -264,51 +524,67 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
     return (t < t1) ? __ldg(prow + t / tiles_per_page) : -1;
   };
   int pid_cur = load_pid(0), pid_next = load_pid(1);
-  uint32_t bad_mask = 0;  // stages whose tile had an invalid page id (warp-uniform)
+  uint32_t bad_mask = 0;  // stages holding an invalid page id (warp-uniform)
 
-  // issue tile k (relative) into stage issued % S; all lanes call
-  auto issue = [&](int k) {
-    if (k > 0 && (k % kPidWin) == 0) {
+  // ---- copy roles: lane = tile * kCopies + kind issues one bulk copy --------
+  const int my_tile = lane / Tr::kCopies, my_kind = lane % Tr::kCopies;
+  const bool copier = lane < TPS * Tr::kCopies;
+  const uint8_t* my_base;
+  long long my_page_stride;
+  int my_tile_stride;
+  uint32_t my_bytes, my_dst;
+  {
+    const long long page_rows = (long long)a.H * a.P;
+    const bool scale_kind = my_kind >= 2;
+    const int rowb = scale_kind ? 8 : Tr::kRow;
+    const uint8_t* pool = my_kind == 0 ? a.kd : my_kind == 1 ? a.vd : my_kind == 2 ? a.ks : a.vs;
+    my_base = pool + (long long)h * a.P * rowb;
+    my_page_stride = page_rows * rowb;
+    my_tile_stride = kTile * rowb;
+    my_bytes = scale_kind ? Tr::kScale : Tr::kData;
+    my_dst = (uint32_t)(my_tile * Tr::kTileBytes) +
+             (my_kind == 0 ? 0u : my_kind == 1 ? (uint32_t)Tr::kData
+                                 : my_kind == 2 ? 2u * Tr::kData : 2u * Tr::kData + Tr::kScale);
+  }
+  int sub = t0 % tiles_per_page;  // tile index within its page of the next chunk's first tile
+
+  // issue chunk c (tiles c*TPS ..) into stage issued % S; all lanes call
+  auto issue = [&](int c) {
+    const int k0 = c * TPS;
+    const int ntc = min(TPS, n - k0);
+    if (k0 > 0 && (k0 % kPidWin) == 0) {
       pid_cur = pid_next;
-      pid_next = load_pid(k / kPidWin + 1);
+      pid_next = load_pid(k0 / kPidWin + 1);
     }
-    const int page = __shfl_sync(0xffffffffu, pid_cur, k % kPidWin);
+    const int page = __shfl_sync(0xffffffffu, pid_cur, (k0 + my_tile) % kPidWin);
     const uint32_t st = ring.issued % S;
     const uint32_t bar = ring.bar + 8 * st;
-    const bool ok = page >= 0 && page < a.num_pages;
+    const bool mine = copier && my_tile < ntc;
+    const bool ok = __all_sync(0xffffffffu, !mine || (page >= 0 && page < a.num_pages));
     bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
-    if (lane == 0) {
-      if (ok) {
-        const int tile = t0 + k;
-        const long long row0 =
-            ((long long)page * a.H + h) * a.P + (long long)(tile % tiles_per_page) * kTile;
-        const uint32_t dst = ring.smem + st * Tr::kStage;
-        mbar_arrive_tx(bar, Tr::kStage);
-        bulk_g2s(dst, a.kd + row0 * Tr::kRow, Tr::kData, bar);
-        bulk_g2s(dst + Tr::kData, a.vd + row0 * Tr::kRow, Tr::kData, bar);
-        if (Tr::kScales) {
-          bulk_g2s(dst + 2 * Tr::kData, a.ks + row0 * 8, Tr::kScale, bar);
-          bulk_g2s(dst + 2 * Tr::kData + Tr::kScale, a.vs + row0 * 8, Tr::kScale, bar);
-        }
-      } else {
-        mbar_arrive_tx(bar, 0);  // completes the phase without data
-      }
+    if (lane == 0) mbar_arrive_tx(bar, ok ? ntc * Tr::kTileBytes : 0);
+    if (ok && mine) {
+      int sb = sub + my_tile;
+      if (sb >= tiles_per_page) sb -= tiles_per_page;
+      bulk_g2s(ring.smem + st * Tr::kStage + my_dst,
+               my_base + (long long)page * my_page_stride + (long long)sb * my_tile_stride, my_bytes, bar);
     }
+    sub += ntc;
+    while (sub >= tiles_per_page) sub -= tiles_per_page;
     ring.issued++;
   };
 
   if (!ring.dead)
-    for (int k = 0; k < min(S, n); ++k) issue(k);
+    for (int c = 0; c < min(S, nch); ++c) issue(c);
 
-  for (int i = 0; i < n; ++i) {
+  for (int c = 0; c < nch; ++c) {
     const uint32_t st = ring.pos % S;
     const uint32_t parity = (ring.pos / S) & 1u;
     if (!ring.dead) {
       uint32_t polls = 0;
       bool ok = mbar_try_wait(ring.bar + 8 * st, parity);
       while (!ok && ++polls < kWaitLimit) ok = mbar_try_wait(ring.bar + 8 * st, parity);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
+      if (!__all_sync(0xffffffffu, ok)) {
         ring.dead = true;
         ring.dead_pos = ring.pos;
         if (lane == 0) atomicOr(a.err, kErrTimeout);
@@ -319,117 +595,47 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
       ring.pos++;
       continue;
     }
-    const uint8_t* sbase = ring.gsmem + st * Tr::kStage;
-    const uint8_t* sK = sbase;
-    const uint8_t* sV = sbase + Tr::kData;
-    const uint8_t* sKs = sbase + 2 * Tr::kData;
-    const uint8_t* sVs = sKs + Tr::kScale;
-    const int tok0 = (t0 + i) * kTile;
-    const int nvalid = min(kTile, T - tok0);
+    const uint8_t* stage = ring.gsmem + st * Tr::kStage;
+    const int ntc = min(TPS, n - c * TPS);
 
-    // ---------------- S = Q K^T (tokens x heads) ----------------
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    float rs0 = 1.f, rs1 = 1.f;  // FP4 block-16 row scales 2^Emax
-    if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
-      const uint4 x0 = lds128(sK + r * 128 + q * 32), x1 = lds128(sK + r * 128 + q * 32 + 16);
-      const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
-      const uint32_t kr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      const uint32_t kr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    // ---- logits of the chunk's tiles ----
+    float sc[TPS][4];
+    int nvalid[TPS];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t a0, a1, a2, a3;
-        if (F == KVQ_FP8_E4M3) {
-          a0 = dec2_e4m3_h2(kr[j]);
-          a2 = dec2_e4m3_h2_hi(kr[j]);
-          a1 = dec2_e4m3_h2(kr8[j]);
-          a3 = dec2_e4m3_h2_hi(kr8[j]);
-        } else {
-          a0 = dec2_e5m2_h2(kr[j]);
-          a2 = dec2_e5m2_h2_hi(kr[j]);
-          a1 = dec2_e5m2_h2(kr8[j]);
-          a3 = dec2_e5m2_h2_hi(kr8[j]);
+    for (int tt = 0; tt < TPS; ++tt) {
+      nvalid[tt] = 0;
+      sc[tt][0] = sc[tt][1] = sc[tt][2] = sc[tt][3] = -INFINITY;
+      if (tt < ntc) {
+        const uint8_t* tb = stage + tt * Tr::kTileBytes;
+        float rs0, rs1;
+        tile_qk<F>(tb, tb + 2 * Tr::kData, r, q, qb, sc[tt], rs0, rs1);
+        sc[tt][0] *= cs0 * rs0;
+        sc[tt][1] *= cs1 * rs0;
+        sc[tt][2] *= cs0 * rs1;
+        sc[tt][3] *= cs1 * rs1;
+        nvalid[tt] = min(kTile, T - (t0 + c * TPS + tt) * kTile);
+        if (nvalid[tt] < kTile) {
+          if (r >= nvalid[tt]) sc[tt][0] = sc[tt][1] = -INFINITY;
+          if (r + 8 >= nvalid[tt]) sc[tt][2] = sc[tt][3] = -INFINITY;
         }
-        mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
-      }
-    } else if (F == KVQ_BF16) {
-      uint32_t kr[16], kr8[16];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 x = lds128(sK + r * 256 + q * 64 + 16 * c);
-        const uint4 y = lds128(sK + (r + 8) * 256 + q * 64 + 16 * c);
-        kr[4 * c] = x.x; kr[4 * c + 1] = x.y; kr[4 * c + 2] = x.z; kr[4 * c + 3] = x.w;
-        kr8[4 * c] = y.x; kr8[4 * c + 1] = y.y; kr8[4 * c + 2] = y.z; kr8[4 * c + 3] = y.w;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) mma_bf16(s, kr[2 * j], kr8[2 * j], kr[2 * j + 1], kr8[2 * j + 1], qb[j][0], qb[j][1]);
-    } else {
-      const uint4 x = lds128(sK + r * 64 + q * 16);
-      const uint4 y = lds128(sK + (r + 8) * 64 + q * 16);
-      const uint32_t sc0 = *reinterpret_cast<const uint16_t*>(sKs + r * 8 + 2 * q);
-      const uint32_t sc1 = *reinterpret_cast<const uint16_t*>(sKs + (r + 8) * 8 + 2 * q);
-      uint32_t f00, f01, f10, f11;  // f16x2 factors: row r / r+8, block 2q / 2q+1
-      if (F == KVQ_NVFP4) {
-        const uint32_t h0 = dec2_e4m3_h2(sc0), h1 = dec2_e4m3_h2(sc1);
-        f00 = __byte_perm(h0, 0, 0x1010);
-        f01 = __byte_perm(h0, 0, 0x3232);
-        f10 = __byte_perm(h1, 0, 0x1010);
-        f11 = __byte_perm(h1, 0, 0x3232);
-      } else {
-        // row maximum exponent over the 8 blocks (4 lanes x 2 blocks)
-        int e0 = max((int)(sc0 & 0xFF), (int)(sc0 >> 8));
-        int e1 = max((int)(sc1 & 0xFF), (int)(sc1 >> 8));
-        e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 1));
-        e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 2));
-        e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 1));
-        e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 2));
-        f00 = h_pow2_nonpos((int)(sc0 & 0xFF) - e0) * 0x10001u;
-        f01 = h_pow2_nonpos((int)(sc0 >> 8) - e0) * 0x10001u;
-        f10 = h_pow2_nonpos((int)(sc1 & 0xFF) - e1) * 0x10001u;
-        f11 = h_pow2_nonpos((int)(sc1 >> 8) - e1) * 0x10001u;
-        rs0 = exp2i(e0 - 127);
-        rs1 = exp2i(e1 - 127);
-      }
-      const uint32_t kw[4] = {x.x, x.y, x.z, x.w}, kw8[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t wr = kw[j >> 1], wr8 = kw8[j >> 1];
-        uint32_t a0, a1, a2, a3;
-        if ((j & 1) == 0) {
-          a0 = e2m1_byte_h2<0>(wr);
-          a2 = e2m1_byte_h2<1>(wr);
-          a1 = e2m1_byte_h2<0>(wr8);
-          a3 = e2m1_byte_h2<1>(wr8);
-        } else {
-          a0 = e2m1_byte_h2<2>(wr);
-          a2 = e2m1_byte_h2<3>(wr);
-          a1 = e2m1_byte_h2<2>(wr8);
-          a3 = e2m1_byte_h2<3>(wr8);
-        }
-        const uint32_t fr = (j < 4) ? f00 : f01, fr8 = (j < 4) ? f10 : f11;
-        a0 = hmul2(a0, fr);
-        a2 = hmul2(a2, fr);
-        a1 = hmul2(a1, fr8);
-        a3 = hmul2(a3, fr8);
-        mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
       }
     }
 
-    // ---------------- online softmax ----------------
-    s[0] *= cs0 * rs0;
-    s[1] *= cs1 * rs0;
-    s[2] *= cs0 * rs1;
-    s[3] *= cs1 * rs1;
-    if (r >= nvalid) s[0] = s[1] = -INFINITY;
-    if (r + 8 >= nvalid) s[2] = s[3] = -INFINITY;
-    float x0 = fmaxf(s[0], s[2]), x1 = fmaxf(s[1], s[3]);
+    // ---- online softmax, rescaling lazily ----
+    float x0 = fmaxf(sc[0][0], sc[0][2]), x1 = fmaxf(sc[0][1], sc[0][3]);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+    for (int tt = 1; tt < TPS; ++tt) {
+      x0 = fmaxf(x0, fmaxf(sc[tt][0], sc[tt][2]));
+      x1 = fmaxf(x1, fmaxf(sc[tt][1], sc[tt][3]));
     }
-    if (__any_sync(0xffffffffu, x0 > m0 || x1 > m1)) {
+    if (__any_sync(0xffffffffu, x0 > m0 + kLazy || x1 > m1 + kLazy)) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      }
       const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-      const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+      const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
       l0 *= al0;
       l1 *= al1;
 #pragma unroll
@@ -442,162 +648,27 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
       m0 = n0;
       m1 = n1;
     }
-    const float p0 = exp2f(s[0] - m0), p1 = exp2f(s[1] - m1);
-    const float p2 = exp2f(s[2] - m0), p3 = exp2f(s[3] - m1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
 
-    // ---------------- O^T += V^T P^T ----------------
-    const int ta = 2 * q, tb = 2 * q + 1, tc = 2 * q + 8, td = 2 * q + 9;
-    const bool partial = nvalid < kTile;
-    if (F == KVQ_BF16) {
-      const uint32_t ph0 = f32x2_to_bf2(p0, p1), ph1 = f32x2_to_bf2(p2, p3);
-      const float l0a = p0 - bf16_bits_to_float(ph0 & 0xFFFF), l1a = p1 - bf16_bits_to_float(ph0 >> 16);
-      const float l2a = p2 - bf16_bits_to_float(ph1 & 0xFFFF), l3a = p3 - bf16_bits_to_float(ph1 >> 16);
-      const uint32_t pl0 = f32x2_to_bf2(l0a, l1a), pl1 = f32x2_to_bf2(l2a, l3a);
-      const uint32_t bh0 = movm_t(ph0), bh1 = movm_t(ph1), bl0 = movm_t(pl0), bl1 = movm_t(pl1);
-      uint32_t va[8], vb[8], vc[8], vd[8];
+    // ---- O^T += V^T P^T ----
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint4 A = lds128(sV + ta * 256 + r * 32 + 16 * c), Bv = lds128(sV + tb * 256 + r * 32 + 16 * c);
-        const uint4 C = lds128(sV + tc * 256 + r * 32 + 16 * c), D = lds128(sV + td * 256 + r * 32 + 16 * c);
-        va[4 * c] = A.x; va[4 * c + 1] = A.y; va[4 * c + 2] = A.z; va[4 * c + 3] = A.w;
-        vb[4 * c] = Bv.x; vb[4 * c + 1] = Bv.y; vb[4 * c + 2] = Bv.z; vb[4 * c + 3] = Bv.w;
-        vc[4 * c] = C.x; vc[4 * c + 1] = C.y; vc[4 * c + 2] = C.z; vc[4 * c + 3] = C.w;
-        vd[4 * c] = D.x; vd[4 * c + 1] = D.y; vd[4 * c + 2] = D.z; vd[4 * c + 3] = D.w;
-      }
-      if (partial) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (ta >= nvalid) va[k] = 0u;
-          if (tb >= nvalid) vb[k] = 0u;
-          if (tc >= nvalid) vc[k] = 0u;
-          if (td >= nvalid) vd[k] = 0u;
-        }
-      }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        // rows: d = 16 r + mt (word mt/2 of the block's first half), d = 16 r + 8 + mt
-        const uint32_t sel = (mt & 1) ? 0x7632u : 0x5410u;
-        const uint32_t a0 = __byte_perm(va[mt >> 1], vb[mt >> 1], sel);
-        const uint32_t a1 = __byte_perm(va[4 + (mt >> 1)], vb[4 + (mt >> 1)], sel);
-        const uint32_t a2 = __byte_perm(vc[mt >> 1], vd[mt >> 1], sel);
-        const uint32_t a3 = __byte_perm(vc[4 + (mt >> 1)], vd[4 + (mt >> 1)], sel);
-        mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
-        mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
-      }
-    } else {
-      const uint32_t b0 = movm_t(f32x2_to_h2(p0, p1)), b1 = movm_t(f32x2_to_h2(p2, p3));
-      if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
-        uint4 A = lds128(sV + ta * 128 + r * 16), Bv = lds128(sV + tb * 128 + r * 16);
-        uint4 C = lds128(sV + tc * 128 + r * 16), D = lds128(sV + td * 128 + r * 16);
-        if (partial) {
-          if (ta >= nvalid) A = make_uint4(0, 0, 0, 0);
-          if (tb >= nvalid) Bv = make_uint4(0, 0, 0, 0);
-          if (tc >= nvalid) C = make_uint4(0, 0, 0, 0);
-          if (td >= nvalid) D = make_uint4(0, 0, 0, 0);
-        }
-        const uint32_t aw[4] = {A.x, A.y, A.z, A.w}, bw[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
-        const uint32_t cw[4] = {C.x, C.y, C.z, C.w}, dw[4] = {D.x, D.y, D.z, D.w};
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          // byte mt (row r) and byte 8 + mt (row r + 8) of each token's block
-          const uint32_t sel = (mt & 2) ? 0x7362u : 0x5140u;
-          const uint32_t pab = __byte_perm(aw[mt >> 2], bw[mt >> 2], sel);
-          const uint32_t pab8 = __byte_perm(aw[2 + (mt >> 2)], bw[2 + (mt >> 2)], sel);
-          const uint32_t pcd = __byte_perm(cw[mt >> 2], dw[mt >> 2], sel);
-          const uint32_t pcd8 = __byte_perm(cw[2 + (mt >> 2)], dw[2 + (mt >> 2)], sel);
-          uint32_t a0, a1, a2, a3;
-          if (F == KVQ_FP8_E4M3) {
-            a0 = (mt & 1) ? dec2_e4m3_h2_hi(pab) : dec2_e4m3_h2(pab);
-            a1 = (mt & 1) ? dec2_e4m3_h2_hi(pab8) : dec2_e4m3_h2(pab8);
-            a2 = (mt & 1) ? dec2_e4m3_h2_hi(pcd) : dec2_e4m3_h2(pcd);
-            a3 = (mt & 1) ? dec2_e4m3_h2_hi(pcd8) : dec2_e4m3_h2(pcd8);
-          } else {
-            a0 = (mt & 1) ? dec2_e5m2_h2_hi(pab) : dec2_e5m2_h2(pab);
-            a1 = (mt & 1) ? dec2_e5m2_h2_hi(pab8) : dec2_e5m2_h2(pab8);
-            a2 = (mt & 1) ? dec2_e5m2_h2_hi(pcd) : dec2_e5m2_h2(pcd);
-            a3 = (mt & 1) ? dec2_e5m2_h2_hi(pcd8) : dec2_e5m2_h2(pcd8);
-          }
-          mma_f16(o[mt], a0, a1, a2, a3, b0, b1);
-        }
-      } else {
-        uint2 A = lds64(sV + ta * 64 + r * 8), Bv = lds64(sV + tb * 64 + r * 8);
-        uint2 C = lds64(sV + tc * 64 + r * 8), D = lds64(sV + td * 64 + r * 8);
-        if (partial) {
-          if (ta >= nvalid) A = make_uint2(0, 0);
-          if (tb >= nvalid) Bv = make_uint2(0, 0);
-          if (tc >= nvalid) C = make_uint2(0, 0);
-          if (td >= nvalid) D = make_uint2(0, 0);
-        }
-        uint32_t sa = sVs[ta * 8 + r], sb = sVs[tb * 8 + r];
-        uint32_t sc = sVs[tc * 8 + r], sd = sVs[td * 8 + r];
-        if (partial) {  // masked tokens: zero codes, and no say in the reference exponent
-          if (ta >= nvalid) sa = 0u;
-          if (tb >= nvalid) sb = 0u;
-          if (tc >= nvalid) sc = 0u;
-          if (td >= nvalid) sd = 0u;
-        }
-        uint32_t fab, fcd;  // f16x2 block factors (token pair)
-        if (F == KVQ_NVFP4) {
-          fab = dec2_e4m3_h2(sa | (sb << 8));
-          fcd = dec2_e4m3_h2(sc | (sd << 8));
-        } else {
-          // running reference exponent of V block r over the tokens seen
-          int et = max(max((int)sa, (int)sb), max((int)sc, (int)sd));
-          et = max(et, __shfl_xor_sync(0xffffffffu, et, 1));
-          et = max(et, __shfl_xor_sync(0xffffffffu, et, 2));
-          if (__any_sync(0xffffffffu, et > vref)) {
-            if (et > vref) {
-              const float f = (vref < -127) ? 0.f : exp2i(vref - et);
-#pragma unroll
-              for (int mt = 0; mt < 8; ++mt) {
-                o[mt][0] *= f;
-                o[mt][1] *= f;
-                o[mt][2] *= f;
-                o[mt][3] *= f;
-              }
-              vref = et;
-            }
-          }
-          fab = h_pow2_nonpos((int)sa - vref) | (h_pow2_nonpos((int)sb - vref) << 16);
-          fcd = h_pow2_nonpos((int)sc - vref) | (h_pow2_nonpos((int)sd - vref) << 16);
-        }
-        // nibble pairs (token a | token b << 4) for even / odd nibble index
-        const uint32_t ev0 = (A.x & 0x0F0F0F0Fu) | ((Bv.x << 4) & 0xF0F0F0F0u);
-        const uint32_t od0 = ((A.x >> 4) & 0x0F0F0F0Fu) | (Bv.x & 0xF0F0F0F0u);
-        const uint32_t ev1 = (A.y & 0x0F0F0F0Fu) | ((Bv.y << 4) & 0xF0F0F0F0u);
-        const uint32_t od1 = ((A.y >> 4) & 0x0F0F0F0Fu) | (Bv.y & 0xF0F0F0F0u);
-        const uint32_t ec0 = (C.x & 0x0F0F0F0Fu) | ((D.x << 4) & 0xF0F0F0F0u);
-        const uint32_t oc0 = ((C.x >> 4) & 0x0F0F0F0Fu) | (D.x & 0xF0F0F0F0u);
-        const uint32_t ec1 = (C.y & 0x0F0F0F0Fu) | ((D.y << 4) & 0xF0F0F0F0u);
-        const uint32_t oc1 = ((C.y >> 4) & 0x0F0F0F0Fu) | (D.y & 0xF0F0F0F0u);
-#define KVQ_PV_TILE(MT, ODD, BYTE)                                                       \
-  {                                                                                     \
-    const uint32_t a0 = hmul2(e2m1_byte_h2<BYTE>(ODD ? od0 : ev0), fab);                \
-    const uint32_t a1 = hmul2(e2m1_byte_h2<BYTE>(ODD ? od1 : ev1), fab);                \
-    const uint32_t a2 = hmul2(e2m1_byte_h2<BYTE>(ODD ? oc0 : ec0), fcd);                \
-    const uint32_t a3 = hmul2(e2m1_byte_h2<BYTE>(ODD ? oc1 : ec1), fcd);                \
-    mma_f16(o[MT], a0, a1, a2, a3, b0, b1);                                             \
-  }
-        KVQ_PV_TILE(0, 0, 0)
-        KVQ_PV_TILE(1, 1, 0)
-        KVQ_PV_TILE(2, 0, 1)
-        KVQ_PV_TILE(3, 1, 1)
-        KVQ_PV_TILE(4, 0, 2)
-        KVQ_PV_TILE(5, 1, 2)
-        KVQ_PV_TILE(6, 0, 3)
-        KVQ_PV_TILE(7, 1, 3)
-#undef KVQ_PV_TILE
+    for (int tt = 0; tt < TPS; ++tt) {
+      if (tt < ntc) {
+        const float p0 = ex2(sc[tt][0] - m0), p1 = ex2(sc[tt][1] - m1);
+        const float p2 = ex2(sc[tt][2] - m0), p3 = ex2(sc[tt][3] - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        const uint8_t* tb = stage + tt * Tr::kTileBytes;
+        tile_pv<F>(tb + Tr::kData, tb + 2 * Tr::kData + Tr::kScale, r, q, nvalid[tt], p0, p1, p2, p3,
+                   o, vref);
       }
     }
 
-    // release the stage and refill it with tile i + S
+    // release the stage and refill it with chunk c + S
     __syncwarp();
     ring.pos++;
-    if (!ring.dead && i + S < n) {
+    if (!ring.dead && c + S < nch) {
       if (lane == 0) fence_proxy_async();
-      issue(i + S);
+      issue(c + S);
     }
   }
 
@@ -671,12 +742,24 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs
       if (T < 0 || T > a.max_pages * a.P) bad_len = true;
       nt = tiles_of(a, b);
     }
+    if (w == 0) {  // publish the per-sequence tile prefix for the merge
+      int incl = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (b < a.B) a.prefix[b + 1] = total + incl;
+    }
     total += warp_sum_i(nt);
   }
   total *= upb;
   if (w == 0) {
     if (__any_sync(0xffffffffu, bad_len) && lane == 0) atomicOr(a.err, kErrRange);
-    if (lane == 0) a.meta[0] = total;
+    if (lane == 0) {
+      a.meta[0] = total;
+      a.prefix[0] = 0;
+    }
   }
   const long long start = worker_start(total, w, a.num_workers);
   const long long end = worker_start(total, w + 1, a.num_workers);
@@ -735,69 +818,70 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs
   }
 }
 
-// One CTA per sequence: combine each (unit, head)'s partials.
+// One CTA per unit, one warp per q head: combine the unit's partials.
 __global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ long long s_red[8];
-  long long part = 0;
-  for (int i = threadIdx.x; i < b; i += blockDim.x) part += tiles_of(a, i);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if (lane == 0) s_red[warp] = part;
-  __syncthreads();
-  long long cum = 0;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) cum += s_red[i];
+  const long long u = blockIdx.x;
+  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long upb = (long long)a.H * a.HG;
-  const long long total = a.meta[0];
+  const int b = (int)(u / upb), ub = (int)(u - (long long)b * upb);
+  const int h = ub / a.HG, hg = ub - (ub / a.HG) * a.HG;
+  if (g >= min(kGroupMax, a.G - hg * kGroupMax)) return;
+  uint16_t* orow = a.out + ((long long)b * a.Hq + h * a.G + hg * kGroupMax + g) * kHeadDim + lane * 4;
   const int nt = tiles_of(a, b);
-  const int nw = a.num_workers;
-  for (int ub = 0; ub < upb; ++ub) {
-    const int h = ub / a.HG, hg = ub % a.HG;
-    const int g = warp;
-    if (g >= min(kGroupMax, a.G - hg * kGroupMax)) continue;
-    uint16_t* orow = a.out + ((long long)b * a.Hq + h * a.G + hg * kGroupMax + g) * kHeadDim + lane * 4;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    bool zero = (nt == 0);
-    if (!zero) {
-      const long long u = (long long)b * upb + ub;
-      const long long w0 = cum * upb + (long long)ub * nt;   // first tile of the unit
-      const long long w1 = w0 + nt;                          // one past its last tile
-      // worker holding tile x: max w with start(w) <= x
-      const int wf = (int)(((w0 + 1) * nw - 1) / total);
-      const int wl = (int)((w1 * nw - 1) / total);
-      float M = -INFINITY;
-      for (int w = wf; w <= wl; ++w) {
-        if (worker_start(total, w, nw) == worker_start(total, w + 1, nw)) continue;
-        const float lse = a.part_lse[(u + w) * kGroupMax + g];
-        if (lse == INFINITY) zero = true;
-        M = fmaxf(M, lse);
-      }
-      if (!zero) {
-        float den = 0.f;
-        for (int w = wf; w <= wl; ++w) {
-          if (worker_start(total, w, nw) == worker_start(total, w + 1, nw)) continue;
-          const long long s = u + w;
-          const float wt = exp2f(a.part_lse[s * kGroupMax + g] - M);
-          const float4 po = *reinterpret_cast<const float4*>(a.part_o + (s * kGroupMax + g) * kHeadDim + lane * 4);
-          den += wt;
-          acc[0] += wt * po.x;
-          acc[1] += wt * po.y;
-          acc[2] += wt * po.z;
-          acc[3] += wt * po.w;
-        }
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] *= inv;
-      }
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (nt > 0) {
+    const long long total = a.meta[0];
+    const int nw = a.num_workers;
+    const long long w0 = a.prefix[b] * upb + (long long)ub * nt;  // first tile of the unit
+    const long long w1 = w0 + nt;                                 // one past its last tile
+    // worker holding tile x: max w with start(w) <= x
+    const int wf = (int)(((w0 + 1) * nw - 1) / total);
+    const int wl = (int)((w1 * nw - 1) / total);
+    float M = -INFINITY;
+    bool poison = false;
+    for (int w = wf + lane; w <= wl; w += 32) {
+      if (worker_start(total, w, nw) == worker_start(total, w + 1, nw)) continue;  // empty worker
+      const float lse = a.part_lse[(u + w) * kGroupMax + g];
+      poison |= (lse == INFINITY);
+      M = fmaxf(M, lse);
     }
-    if (zero) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-    uint2 ov;
-    ov.x = bf16_rne_bits(acc[0]) | (bf16_rne_bits(acc[1]) << 16);
-    ov.y = bf16_rne_bits(acc[2]) | (bf16_rne_bits(acc[3]) << 16);
-    *reinterpret_cast<uint2*>(orow) = ov;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    poison = __any_sync(0xffffffffu, poison);
+    if (!poison) {
+      float den = 0.f;
+      for (int c0 = wf; c0 <= wl; c0 += 32) {
+        const int w = c0 + lane;
+        float wt = 0.f;
+        if (w <= wl && worker_start(total, w, nw) != worker_start(total, w + 1, nw))
+          wt = ex2(a.part_lse[(u + w) * kGroupMax + g] - M);
+        den += wt;
+        const int cnt = min(32, wl - c0 + 1);
+#pragma unroll 4
+        for (int j = 0; j < cnt; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, wt, j);
+          if (wj != 0.f) {
+            const float4 po = *reinterpret_cast<const float4*>(
+                a.part_o + ((u + c0 + j) * kGroupMax + g) * kHeadDim + lane * 4);
+            acc[0] += wj * po.x;
+            acc[1] += wj * po.y;
+            acc[2] += wj * po.z;
+            acc[3] += wj * po.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      const float inv = 1.f / den;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] *= inv;
+    }
   }
+  uint2 ov;
+  ov.x = bf16_rne_bits(acc[0]) | (bf16_rne_bits(acc[1]) << 16);
+  ov.y = bf16_rne_bits(acc[2]) | (bf16_rne_bits(acc[3]) << 16);
+  *reinterpret_cast<uint2*>(orow) = ov;
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -867,7 +951,8 @@ bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_pe
   plan->num_workers = plan->ctas * kWarpsPerCta;
   plan->num_slots = plan->num_units + plan->num_workers;
   plan->ws_bytes = align256((size_t)plan->num_slots * kGroupMax * kHeadDim * sizeof(float)) +
-                   align256((size_t)plan->num_slots * kGroupMax * sizeof(float)) + 256;
+                   align256((size_t)plan->num_slots * kGroupMax * sizeof(float)) + 256 +
+                   align256((size_t)(batch + 1) * sizeof(long long));
   return true;
 }
 
@@ -883,6 +968,8 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
   a.part_lse = reinterpret_cast<float*>(ws);
   ws += align256((size_t)plan.num_slots * kGroupMax * sizeof(float));
   a.meta = reinterpret_cast<long long*>(ws);
+  ws += 256;
+  a.prefix = reinterpret_cast<long long*>(ws);
   a.q = static_cast<const uint16_t*>(q);
   a.out = static_cast<uint16_t*>(out);
   a.page_table = page_table;
@@ -915,7 +1002,7 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
   if (e != cudaSuccess) return e;
   // merge: programmatic dependent launch (starts while the split kernel drains)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(batch);
+  cfg.gridDim = dim3((unsigned)plan.num_units);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
