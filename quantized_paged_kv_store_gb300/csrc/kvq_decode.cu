@@ -42,6 +42,7 @@
 #include "kvq_internal.h"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace kvq {
 namespace {
@@ -598,14 +599,15 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
     const uint8_t* stage = ring.gsmem + st * Tr::kStage;
     const int ntc = min(TPS, n - c * TPS);
 
-    // ---- logits of the chunk's tiles ----
-    float sc[TPS][4];
-    int nvalid[TPS];
+    // One chunk of NT tiles; NT is a compile-time constant so the tiles'
+    // independent dequant/MMA chains can be interleaved by the compiler.
+    auto run_chunk = [&](auto nt_const) {
+      constexpr int NT = decltype(nt_const)::value;
+      // ---- logits of the chunk's tiles ----
+      float sc[NT][4];
+      int nvalid[NT];
 #pragma unroll
-    for (int tt = 0; tt < TPS; ++tt) {
-      nvalid[tt] = 0;
-      sc[tt][0] = sc[tt][1] = sc[tt][2] = sc[tt][3] = -INFINITY;
-      if (tt < ntc) {
+      for (int tt = 0; tt < NT; ++tt) {
         const uint8_t* tb = stage + tt * Tr::kTileBytes;
         float rs0, rs1;
         tile_qk<F>(tb, tb + 2 * Tr::kData, r, q, qb, sc[tt], rs0, rs1);
@@ -619,40 +621,38 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
           if (r + 8 >= nvalid[tt]) sc[tt][2] = sc[tt][3] = -INFINITY;
         }
       }
-    }
 
-    // ---- online softmax, rescaling lazily ----
-    float x0 = fmaxf(sc[0][0], sc[0][2]), x1 = fmaxf(sc[0][1], sc[0][3]);
+      // ---- online softmax, rescaling lazily ----
+      float x0 = fmaxf(sc[0][0], sc[0][2]), x1 = fmaxf(sc[0][1], sc[0][3]);
 #pragma unroll
-    for (int tt = 1; tt < TPS; ++tt) {
-      x0 = fmaxf(x0, fmaxf(sc[tt][0], sc[tt][2]));
-      x1 = fmaxf(x1, fmaxf(sc[tt][1], sc[tt][3]));
-    }
-    if (__any_sync(0xffffffffu, x0 > m0 + kLazy || x1 > m1 + kLazy)) {
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      for (int tt = 1; tt < NT; ++tt) {
+        x0 = fmaxf(x0, fmaxf(sc[tt][0], sc[tt][2]));
+        x1 = fmaxf(x1, fmaxf(sc[tt][1], sc[tt][3]));
       }
-      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-      const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
-      l0 *= al0;
-      l1 *= al1;
+      if (__any_sync(0xffffffffu, x0 > m0 + kLazy || x1 > m1 + kLazy)) {
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
+        for (int off = 4; off < 32; off <<= 1) {
+          x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+          x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+        }
+        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+        const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
+        l0 *= al0;
+        l1 *= al1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= al0;
+          o[mt][1] *= al1;
+          o[mt][2] *= al0;
+          o[mt][3] *= al1;
+        }
+        m0 = n0;
+        m1 = n1;
       }
-      m0 = n0;
-      m1 = n1;
-    }
 
-    // ---- O^T += V^T P^T ----
+      // ---- O^T += V^T P^T ----
 #pragma unroll
-    for (int tt = 0; tt < TPS; ++tt) {
-      if (tt < ntc) {
+      for (int tt = 0; tt < NT; ++tt) {
         const float p0 = ex2(sc[tt][0] - m0), p1 = ex2(sc[tt][1] - m1);
         const float p2 = ex2(sc[tt][2] - m0), p3 = ex2(sc[tt][3] - m1);
         l0 += p0 + p2;
@@ -661,7 +661,11 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         tile_pv<F>(tb + Tr::kData, tb + 2 * Tr::kData + Tr::kScale, r, q, nvalid[tt], p0, p1, p2, p3,
                    o, vref);
       }
-    }
+    };
+    if (ntc == TPS)
+      run_chunk(std::integral_constant<int, TPS>{});
+    else
+      run_chunk(std::integral_constant<int, 1>{});
 
     // release the stage and refill it with chunk c + S
     __syncwarp();
