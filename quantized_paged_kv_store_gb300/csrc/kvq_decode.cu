@@ -212,6 +212,7 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
     const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
     const uint32_t kr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     const uint32_t kr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: two independent MMA chains
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t a0, a1, a2, a3;
@@ -226,8 +227,12 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
         a1 = dec2_e5m2_h2(kr8[j]);
         a3 = dec2_e5m2_h2_hi(kr8[j]);
       }
-      mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+      mma_f16((j & 1) ? s2 : s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
     }
+    s[0] += s2[0];
+    s[1] += s2[1];
+    s[2] += s2[2];
+    s[3] += s2[3];
   } else if (F == KVQ_BF16) {
     uint32_t kr[16], kr8[16];
 #pragma unroll
@@ -267,6 +272,7 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
       rs1 = exp2i(e1 - 127);
     }
     const uint32_t kw[4] = {x.x, x.y, x.z, x.w}, kw8[4] = {y.x, y.y, y.z, y.w};
+    float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: two independent MMA chains
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t wr = kw[j >> 1], wr8 = kw8[j >> 1];
@@ -287,8 +293,12 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
       a2 = hmul2(a2, fr);
       a1 = hmul2(a1, fr8);
       a3 = hmul2(a3, fr8);
-      mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+      mma_f16((j & 1) ? s2 : s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
     }
+    s[0] += s2[0];
+    s[1] += s2[1];
+    s[2] += s2[2];
+    s[3] += s2[3];
   }
 
 }
@@ -483,7 +493,7 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         qb[j][0] = w16[2 * j];
         qb[j][1] = w16[2 * j + 1];
       }
-      colscale = (r < gh) ? a.qscale : 0.f;
+      colscale = (r < gh) ? a.qscale : 1.f;  // padded heads: zero q, any positive scale
     } else {
       float amax = 0.f;
 #pragma unroll
@@ -503,7 +513,7 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         qb[j][1] = f32x2_to_h2(bf16_bits_to_float(w16[2 * j + 1] & 0xFFFF) * mul,
                                bf16_bits_to_float(w16[2 * j + 1] >> 16) * mul);
       }
-      colscale = (r < gh) ? a.qscale * exp2i(sq) : 0.f;
+      colscale = (r < gh) ? a.qscale * exp2i(sq) : 1.f;
     }
   }
   // D1 columns of this thread are heads 2q, 2q+1 (held by lanes 8q and 8q+4 above)
@@ -611,10 +621,12 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         const uint8_t* tb = stage + tt * Tr::kTileBytes;
         float rs0, rs1;
         tile_qk<F>(tb, tb + 2 * Tr::kData, r, q, qb, sc[tt], rs0, rs1);
-        sc[tt][0] *= cs0 * rs0;
-        sc[tt][1] *= cs1 * rs0;
-        sc[tt][2] *= cs0 * rs1;
-        sc[tt][3] *= cs1 * rs1;
+        if (F == KVQ_FP4_BLOCK16) {  // per-row 2^Emax factors
+          sc[tt][0] *= rs0;
+          sc[tt][1] *= rs0;
+          sc[tt][2] *= rs1;
+          sc[tt][3] *= rs1;
+        }
         nvalid[tt] = min(kTile, T - (t0 + c * TPS + tt) * kTile);
         if (nvalid[tt] < kTile) {
           if (r >= nvalid[tt]) sc[tt][0] = sc[tt][1] = -INFINITY;
@@ -622,13 +634,15 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         }
       }
 
-      // ---- online softmax, rescaling lazily ----
+      // ---- online softmax on scaled logits cs * s (cs > 0), rescaling lazily ----
       float x0 = fmaxf(sc[0][0], sc[0][2]), x1 = fmaxf(sc[0][1], sc[0][3]);
 #pragma unroll
       for (int tt = 1; tt < NT; ++tt) {
         x0 = fmaxf(x0, fmaxf(sc[tt][0], sc[tt][2]));
         x1 = fmaxf(x1, fmaxf(sc[tt][1], sc[tt][3]));
       }
+      x0 *= cs0;
+      x1 *= cs1;
       if (__any_sync(0xffffffffu, x0 > m0 + kLazy || x1 > m1 + kLazy)) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -653,8 +667,8 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
       // ---- O^T += V^T P^T ----
 #pragma unroll
       for (int tt = 0; tt < NT; ++tt) {
-        const float p0 = ex2(sc[tt][0] - m0), p1 = ex2(sc[tt][1] - m1);
-        const float p2 = ex2(sc[tt][2] - m0), p3 = ex2(sc[tt][3] - m1);
+        const float p0 = ex2(fmaf(sc[tt][0], cs0, -m0)), p1 = ex2(fmaf(sc[tt][1], cs1, -m1));
+        const float p2 = ex2(fmaf(sc[tt][2], cs0, -m0)), p3 = ex2(fmaf(sc[tt][3], cs1, -m1));
         l0 += p0 + p2;
         l1 += p1 + p3;
         const uint8_t* tb = stage + tt * Tr::kTileBytes;
