@@ -51,7 +51,7 @@ constexpr int kWarpsPerCta = 4;
 constexpr int kHeadDim = 128;
 constexpr int kTile = 16;      // tokens per tile
 constexpr int kGroupMax = 8;   // q heads per unit
-constexpr int kPidWin = 32;    // page ids prefetched per window
+constexpr int kPidWin = 30;    // page ids prefetched per window (a multiple of every stage size)
 constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before giving up (~1 s)
 
 template <kvq_format F>
@@ -62,7 +62,7 @@ struct Traits {
   static constexpr int kScale = kScales ? kTile * 8 : 0;  // its block scales
   static constexpr int kTileBytes = 2 * (kData + kScale); // K, V (+ scales) of one tile
   static constexpr int kCopies = kScales ? 4 : 2;         // bulk copies per tile
-  static constexpr int kTps = (F == KVQ_BF16) ? 1 : 2;    // tiles per stage
+  static constexpr int kTps = (F == KVQ_BF16) ? 1 : (F == KVQ_NVFP4 || F == KVQ_FP4_BLOCK16) ? 3 : 2;
   static constexpr int kStage = kTps * kTileBytes;
   static constexpr int kStages = (F == KVQ_BF16) ? 3 : 2;
   static constexpr int kWarpSmem = kStages * kStage;
@@ -164,11 +164,13 @@ __device__ __forceinline__ float ex2(float x) {
   return r;
 }
 
-// f16 bits of 2^d for d <= 0 (exact down to 2^-24, 0 below).
-__device__ __forceinline__ uint32_t h_pow2_nonpos(int d) {
-  if (d >= -14) return (uint32_t)(d + 15) << 10;
-  if (d >= -24) return 1u << (d + 24);
-  return 0u;
+// half2 of (2^da, 2^db) for da, db <= 0: exact down to 2^-24 (f16 subnormals
+// included), 0 below.  Built as fp32 powers of two (exponent field, clamped
+// at 2^-126) and rounded to f16 by one convert.
+__device__ __forceinline__ uint32_t h2_pow2_nonpos(int da, int db) {
+  const float fa = __uint_as_float((uint32_t)(max(da, -126) + 127) << 23);
+  const float fb = __uint_as_float((uint32_t)(max(db, -126) + 127) << 23);
+  return f32x2_to_h2(fa, fb);
 }
 
 __device__ __forceinline__ int warp_sum_i(int v) {
@@ -264,10 +266,12 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
       e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 2));
       e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 1));
       e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 2));
-      f00 = h_pow2_nonpos((int)(sc0 & 0xFF) - e0) * 0x10001u;
-      f01 = h_pow2_nonpos((int)(sc0 >> 8) - e0) * 0x10001u;
-      f10 = h_pow2_nonpos((int)(sc1 & 0xFF) - e1) * 0x10001u;
-      f11 = h_pow2_nonpos((int)(sc1 >> 8) - e1) * 0x10001u;
+      const uint32_t h0 = h2_pow2_nonpos((int)(sc0 & 0xFF) - e0, (int)(sc0 >> 8) - e0);
+      const uint32_t h1 = h2_pow2_nonpos((int)(sc1 & 0xFF) - e1, (int)(sc1 >> 8) - e1);
+      f00 = __byte_perm(h0, 0, 0x1010);
+      f01 = __byte_perm(h0, 0, 0x3232);
+      f10 = __byte_perm(h1, 0, 0x1010);
+      f11 = __byte_perm(h1, 0, 0x3232);
       rs0 = exp2i(e0 - 127);
       rs1 = exp2i(e1 - 127);
     }
@@ -421,8 +425,8 @@ __device__ __forceinline__ void tile_pv(const uint8_t* sV, const uint8_t* sVs, i
             vref = et;
           }
         }
-        fab = h_pow2_nonpos((int)sa - vref) | (h_pow2_nonpos((int)sb - vref) << 16);
-        fcd = h_pow2_nonpos((int)sc - vref) | (h_pow2_nonpos((int)sd - vref) << 16);
+        fab = h2_pow2_nonpos((int)sa - vref, (int)sb - vref);
+        fcd = h2_pow2_nonpos((int)sc - vref, (int)sd - vref);
       }
       // nibble pairs (token a | token b << 4) for even / odd nibble index
       const uint32_t ev0 = (A.x & 0x0F0F0F0Fu) | ((Bv.x << 4) & 0xF0F0F0F0u);
@@ -575,8 +579,8 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
     bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
     if (lane == 0) mbar_arrive_tx(bar, ok ? ntc * Tr::kTileBytes : 0);
     if (ok && mine) {
-      int sb = sub + my_tile;
-      if (sb >= tiles_per_page) sb -= tiles_per_page;
+      int sb = sub + my_tile;  // my_tile < TPS <= 3: at most two wraps
+      while (sb >= tiles_per_page) sb -= tiles_per_page;
       bulk_g2s(ring.smem + st * Tr::kStage + my_dst,
                my_base + (long long)page * my_page_stride + (long long)sb * my_tile_stride, my_bytes, bar);
     }
@@ -676,10 +680,14 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
                    o, vref);
       }
     };
-    if (ntc == TPS)
+    if (ntc == TPS) {
       run_chunk(std::integral_constant<int, TPS>{});
-    else
+    } else if (ntc == 1) {
       run_chunk(std::integral_constant<int, 1>{});
+    } else {
+      if constexpr (TPS >= 3) run_chunk(std::integral_constant<int, 2>{});  // 2-tile tail of a 3-tile stage
+    }
+    static_assert(TPS <= 3, "chunk tails above 2 tiles need their own case");
 
     // release the stage and refill it with chunk c + S
     __syncwarp();

@@ -121,3 +121,41 @@ def test_decode_deterministic_and_workspace_checks(kvq, cuda):
     with pytest.raises(kvq.KVQError) as e:
         cbad.workspace_size(1, 4, 4)
     assert e.value.code == "KVQ_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("spread", [10, 20, 30])
+def test_fp4_block16_wide_exponent_spread(kvq, orc, cuda, spread):
+    """K and V rows whose 16-element blocks differ by up to 2^spread: inside the
+    kernel each K block is held relative to its row's largest block and each V
+    block relative to the largest seen so far (f16 subnormals down to 2^-24,
+    smaller contributions flush); the result must stay within tolerance."""
+    wl = synth.make_workload("spread", "fp4_mx_block16", Hq=16, Hkv=2, seq_lens=[70, 33], seed=spread)
+    rng = np.random.default_rng(spread)
+    mult = 2.0 ** (-spread * (np.arange(8) % 2)) * 2.0 ** rng.integers(-3, 4, size=8)
+    ks, vs = [], []
+    for b in range(wl.B):
+        k, v = wl.kv_float(0, b)
+        k = k * torch.from_numpy(np.repeat(mult, 16)).float()
+        v = v * torch.from_numpy(np.repeat(mult[::-1].copy(), 16)).float()
+        ks.append(synth.to_bf16_bits(k))
+        vs.append(synth.to_bf16_bits(v))
+    c = gpu_cache_for(kvq, wl)
+    oc = orc.OracleCache(wl.fmt, wl.Hkv, wl.D, wl.P, wl.num_pages)
+    for b in range(wl.B):
+        c.quantize_and_store(0, bits_to_cuda(ks[b]), bits_to_cuda(vs[b]),
+                             torch.from_numpy(wl.slots(b)).cuda(), None)
+        assert oc.quantize_store(ks[b], vs[b], wl.slots(b), None) == 0
+    got = gpu_decode(c, wl)
+    ref, rc = oc.decode_attention(wl.q(), wl.page_table, wl.seq_lens, wl.sm_scale)
+    assert rc == 0 and c.device_error() == 0
+    assert_attention_close(got, ref, f"fp4 block-16 spread 2^{spread}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("L,P", [(34, 16), (48, 16), (49, 16), (100, 32), (200, 64), (47, 48)])
+def test_decode_whole_stages_per_worker(kvq, orc, cuda, fmt, L, P):
+    """Eight equal sequences over one kv head: each worker gets whole multi-tile
+    stages (page slabs of 1 to 4 tiles, full and partial last tiles)."""
+    wl = synth.make_workload(f"w_{fmt}", fmt, Hq=8, Hkv=1, P=P, seq_lens=[L] * 8, seed=L + P)
+    got, ref = _run(kvq, orc, wl)
+    assert_attention_close(got, ref, f"{fmt} L={L} P={P}")
