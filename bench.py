@@ -119,7 +119,7 @@ def peak_hbm():
 
 def decode_source_hash():
     h = hashlib.sha256()
-    for n in ("kvq_decode.cu", "kvq_codecs.cuh"):
+    for n in ("kvq_decode.cu", "kvq_decode_args.cuh", "kvq_codecs.cuh"):
         with open(os.path.join(ROOT, "quantized_paged_kv_store_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -39,6 +39,7 @@
 // a high and a low bf16 part.  Per-tensor scales fold into the logit scale
 // (K) and the output (V).  Accumulation is fp32.
 #include "kvq_codecs.cuh"
+#include "kvq_decode_args.cuh"
 #include "kvq_internal.h"
 
 #include <algorithm>
@@ -48,9 +49,6 @@ namespace kvq {
 namespace {
 
 constexpr int kWarpsPerCta = 4;
-constexpr int kHeadDim = 128;
-constexpr int kTile = 16;      // tokens per tile
-constexpr int kGroupMax = 8;   // q heads per unit
 constexpr int kPidWin = 30;    // page ids prefetched per window (a multiple of every stage size)
 constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before giving up (~1 s)
 
@@ -67,27 +65,6 @@ struct Traits {
   static constexpr int kStages = (F == KVQ_BF16) ? 3 : 2;
   static constexpr int kWarpSmem = kStages * kStage;
   static constexpr int kCtaSmem = kWarpsPerCta * (kWarpSmem + kStages * 8);
-};
-
-struct DecodeArgs {
-  const uint16_t* q;
-  uint16_t* out;
-  const int32_t* page_table;
-  const int32_t* seq_lens;
-  const uint8_t* kd;
-  const uint8_t* vd;
-  const uint8_t* ks;
-  const uint8_t* vs;
-  float* part_o;      // [slots][8][128]
-  float* part_lse;    // [slots][8]
-  long long* meta;    // [0] = Wtot
-  long long* prefix;  // [B + 1]: tiles of sequences before b (written by worker 0)
-  int B, H, Hq, G, HG, max_pages, P;
-  long long num_pages;
-  int num_workers;
-  float qscale;       // sm_scale * log2(e) * (k_scale | g_k | 1)
-  float v_factor;     // v_scale | g_v | 1
-  int* err;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -156,14 +133,6 @@ __device__ __forceinline__ uint32_t f32x2_to_bf2(float lo, float hi) {
 template <int K>
 __device__ __forceinline__ uint32_t e2m1_byte_h2(uint32_t x) { return dec2_e2m1_h2<K>(x); }
 
-// 2^x by the hardware approximation; results below 2^-126 flush to zero,
-// which is harmless for softmax weights that small.
-__device__ __forceinline__ float ex2(float x) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
 // half2 of (2^da, 2^db) for da, db <= 0: exact down to 2^-24 (f16 subnormals
 // included), 0 below.  Built as fp32 powers of two (exponent field, clamped
 // at 2^-126) and rounded to f16 by one convert.
@@ -177,17 +146,6 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
-}
-
-// Tiles of sequence b (0 for an empty or invalid length).
-__device__ __forceinline__ int tiles_of(const DecodeArgs& a, int b) {
-  const int T = __ldg(a.seq_lens + b);
-  return (T > 0 && T <= a.max_pages * a.P) ? (T + kTile - 1) / kTile : 0;
-}
-
-// First tile of worker w (integer split of [0, total)).
-__device__ __forceinline__ long long worker_start(long long total, int w, int nw) {
-  return total * w / nw;
 }
 
 // Per-warp staging ring.
@@ -844,72 +802,6 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs
   }
 }
 
-// One CTA per unit, one warp per q head: combine the unit's partials.
-__global__ void __launch_bounds__(256) merge_kernel(DecodeArgs a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const long long u = blockIdx.x;
-  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long upb = (long long)a.H * a.HG;
-  const int b = (int)(u / upb), ub = (int)(u - (long long)b * upb);
-  const int h = ub / a.HG, hg = ub - (ub / a.HG) * a.HG;
-  if (g >= min(kGroupMax, a.G - hg * kGroupMax)) return;
-  uint16_t* orow = a.out + ((long long)b * a.Hq + h * a.G + hg * kGroupMax + g) * kHeadDim + lane * 4;
-  const int nt = tiles_of(a, b);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (nt > 0) {
-    const long long total = a.meta[0];
-    const int nw = a.num_workers;
-    const long long w0 = a.prefix[b] * upb + (long long)ub * nt;  // first tile of the unit
-    const long long w1 = w0 + nt;                                 // one past its last tile
-    // worker holding tile x: max w with start(w) <= x
-    const int wf = (int)(((w0 + 1) * nw - 1) / total);
-    const int wl = (int)((w1 * nw - 1) / total);
-    float M = -INFINITY;
-    bool poison = false;
-    for (int w = wf + lane; w <= wl; w += 32) {
-      if (worker_start(total, w, nw) == worker_start(total, w + 1, nw)) continue;  // empty worker
-      const float lse = a.part_lse[(u + w) * kGroupMax + g];
-      poison |= (lse == INFINITY);
-      M = fmaxf(M, lse);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    poison = __any_sync(0xffffffffu, poison);
-    if (!poison) {
-      float den = 0.f;
-      for (int c0 = wf; c0 <= wl; c0 += 32) {
-        const int w = c0 + lane;
-        float wt = 0.f;
-        if (w <= wl && worker_start(total, w, nw) != worker_start(total, w + 1, nw))
-          wt = ex2(a.part_lse[(u + w) * kGroupMax + g] - M);
-        den += wt;
-        const int cnt = min(32, wl - c0 + 1);
-#pragma unroll 4
-        for (int j = 0; j < cnt; ++j) {
-          const float wj = __shfl_sync(0xffffffffu, wt, j);
-          if (wj != 0.f) {
-            const float4 po = *reinterpret_cast<const float4*>(
-                a.part_o + ((u + c0 + j) * kGroupMax + g) * kHeadDim + lane * 4);
-            acc[0] += wj * po.x;
-            acc[1] += wj * po.y;
-            acc[2] += wj * po.z;
-            acc[3] += wj * po.w;
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      const float inv = 1.f / den;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] *= inv;
-    }
-  }
-  uint2 ov;
-  ov.x = bf16_rne_bits(acc[0]) | (bf16_rne_bits(acc[1]) << 16);
-  ov.y = bf16_rne_bits(acc[2]) | (bf16_rne_bits(acc[3]) << 16);
-  *reinterpret_cast<uint2*>(orow) = ov;
-}
-
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 template <kvq_format F>
@@ -1026,18 +918,7 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
     case KVQ_NVFP4: e = launch_f<KVQ_NVFP4>(a, plan.ctas, stream); break;
   }
   if (e != cudaSuccess) return e;
-  // merge: programmatic dependent launch (starts while the split kernel drains)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)plan.num_units);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel, a);
+  return launch_merge(a, plan.num_units, stream);
 }
 
 }  // namespace kvq
