@@ -59,6 +59,8 @@ def parse_args(argv=None):
     p.add_argument("--seed", type=int, default=1004)
     p.add_argument("--sweep", default=None, help="also run the format x context x batch sweep, "
                    "one JSON line per cell appended to this file")
+    p.add_argument("--store", default=None, help="also time quantize-and-store of the 70B-layer "
+                   "16K x 8 prefill in every format, one JSON line per format appended to this file")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=32,
@@ -407,7 +409,55 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if args.sweep:
         run_sweep(args)
+    if args.store:
+        run_store(args)
     barrier()
+
+
+def run_store(args, steps=200, warmup=10):
+    """Quantize-and-store throughput: the 70B-layer prefill of 8 sequences x 16K
+    tokens (K and V, 8 kv heads, head_dim 128) stored in one call per step.
+    Algorithmic bytes: bf16 K and V read, slot ids read, cache rows and block
+    scales written."""
+    import numpy as np
+    import torch
+    import quantized_paged_kv_store_gb300 as kvq
+    import synth
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    wl = synth.cfg3_fp4b16_70b(seed=args.seed + 7919 * rank)
+    ks, vs = wl.kv_all(0)
+    k = synth_to_cuda(np.concatenate(ks))
+    v = synth_to_cuda(np.concatenate(vs))
+    slots = torch.from_numpy(np.concatenate([wl.slots(b) for b in range(wl.B)])).to(dev)
+    n = int(slots.shape[0])
+    peak, _ = peak_hbm()
+    for fmt in ("nvfp4", "fp4_mx_block16", "fp8_e4m3", "fp8_e5m2", "bf16"):
+        wl.fmt = fmt
+        scales = [float(x) for x in wl._scales_from(ks, vs)]
+        cache = kvq.KVQCache(fmt, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
+        for _ in range(warmup):
+            cache.quantize_and_store(0, k, v, slots, scales)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record()
+        for i in range(steps):
+            cache.quantize_and_store(0, k, v, slots, scales)
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        ms = statistics.fmean(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+        if cache.device_error() != 0:
+            raise RuntimeError("device error during the store benchmark")
+        row_w = {"bf16": 256, "fp8_e4m3": 128, "fp8_e5m2": 128}.get(fmt, 64 + 8)
+        nbytes = n * wl.Hkv * (2 * wl.D * 2 + 2 * row_w) + n * 8
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        cache.close()
+        if rank == 0:
+            with open(args.store, "a") as f:
+                f.write(json.dumps({"kernel": "quantize-and-store", "format": fmt, "tokens": n,
+                                    "kv_heads": wl.Hkv, "head_dim": wl.D, "us_per_call": round(ms * 1e3, 2),
+                                    "bytes_per_call": nbytes, "GBps": round(gbs, 1),
+                                    "frac": round(gbs / peak, 4)}) + "\n")
 
 
 def run_sweep(args):
