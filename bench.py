@@ -61,6 +61,9 @@ def parse_args(argv=None):
                    "one JSON line per cell appended to this file")
     p.add_argument("--store", default=None, help="also time quantize-and-store of the 70B-layer "
                    "16K x 8 prefill in every format, one JSON line per format appended to this file")
+    p.add_argument("--store-formats", default=None, help="comma-separated subset for --store")
+    p.add_argument("--store-only", action="store_true",
+                   help="run only the --store measurement (no decode line)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=32,
@@ -414,7 +417,7 @@ def run_ours(args):
     barrier()
 
 
-def run_store(args, steps=200, warmup=10):
+def run_store(args, steps=None, warmup=None):
     """Quantize-and-store throughput: the 70B-layer prefill of 8 sequences x 16K
     tokens (K and V, 8 kv heads, head_dim 128) stored in one call per step.
     Algorithmic bytes: bf16 K and V read, slot ids read, cache rows and block
@@ -432,7 +435,10 @@ def run_store(args, steps=200, warmup=10):
     slots = torch.from_numpy(np.concatenate([wl.slots(b) for b in range(wl.B)])).to(dev)
     n = int(slots.shape[0])
     peak, _ = peak_hbm()
-    for fmt in ("nvfp4", "fp4_mx_block16", "fp8_e4m3", "fp8_e5m2", "bf16"):
+    steps = steps or max(5, min(args.steps, 200))
+    warmup = warmup or max(3, min(args.warmup, 10))
+    for fmt in (("nvfp4", "fp4_mx_block16", "fp8_e4m3", "fp8_e5m2", "bf16") if args.store_formats is None
+                else args.store_formats.split(",")):
         wl.fmt = fmt
         scales = [float(x) for x in wl._scales_from(ks, vs)]
         cache = kvq.KVQCache(fmt, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
@@ -539,6 +545,9 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.store_only:
+        run_store(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -143,3 +143,52 @@ def test_prefill_16k_fp4_block16_sampled(kvq, orc, cuda):
         rows = np.array([oc.row_index(int(s), h) for s in wl.slots(b) for h in range(wl.Hkv)])
         assert np.array_equal(gk[rows], oc.k_data[rows]) and np.array_equal(gv[rows], oc.v_data[rows])
         assert np.array_equal(gks[rows], oc.k_scales[rows]) and np.array_equal(gvs[rows], oc.v_scales[rows])
+
+
+def _all_finite_bf16(shuffle_seed=0):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = (bits & 0x7F80) != 0x7F80
+    bits = bits[finite]
+    return np.random.default_rng(shuffle_seed).permutation(bits)
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("scale", [1.0, 0.37, 3.0, 1.0 / 3.0, 0.0137, 2.0 ** -70, 2.0 ** -90, 1e30])
+def test_fp8_store_every_bf16_value(kvq, orc, cuda, fmt, scale):
+    """Every finite bf16 input, quantized with per-tensor scales that make the
+    fp32 quotient exact, inexact, tiny, huge or overflowing: the kernel's
+    division must round exactly like IEEE fp32 division (the oracle's)."""
+    D = 64
+    bits = _all_finite_bf16(1)
+    n = bits.size // D
+    x = bits[: n * D].reshape(n, 1, D)
+    P = 16
+    num_pages = (n + P - 1) // P
+    slots = np.arange(n, dtype=np.int64)
+    c = kvq.KVQCache(fmt, 1, 1, D, P, num_pages)
+    c.quantize_and_store(0, bits_to_cuda(x), bits_to_cuda(x[::-1].copy()), torch.from_numpy(slots).cuda(),
+                         [scale, scale * 1.5])
+    oc = orc.OracleCache(fmt, 1, D, P, num_pages)
+    assert oc.quantize_store(x, x[::-1].copy(), slots, [scale, scale * 1.5]) == 0
+    _assert_pools_equal(gpu_pools(c, 0), oc, fmt)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp4_mx_block16"])
+@pytest.mark.parametrize("g", [0.0137, 1.0, 3.0e-5, 2.0 ** -85])
+def test_fp4_store_every_bf16_value(kvq, orc, cuda, fmt, g):
+    """Every finite bf16 input, in 16-element blocks of mixed magnitude: block
+    scales and codes must match the oracle byte for byte."""
+    D = 128
+    bits = _all_finite_bf16(2)
+    n = bits.size // D
+    x = bits[: n * D].reshape(n, 1, D)
+    P = 16
+    num_pages = (n + P - 1) // P
+    slots = np.arange(n, dtype=np.int64)
+    c = kvq.KVQCache(fmt, 1, 1, D, P, num_pages)
+    scales = [g, g * 7.0] if fmt == "nvfp4" else None
+    c.quantize_and_store(0, bits_to_cuda(x), bits_to_cuda(x[::-1].copy()), torch.from_numpy(slots).cuda(),
+                         scales)
+    oc = orc.OracleCache(fmt, 1, D, P, num_pages)
+    assert oc.quantize_store(x, x[::-1].copy(), slots, scales) == 0
+    _assert_pools_equal(gpu_pools(c, 0), oc, fmt)
