@@ -572,9 +572,11 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
     const int ntc = min(TPS, n - c * TPS);
 
     // One chunk of NT tiles; NT is a compile-time constant so the tiles'
-    // independent dequant/MMA chains can be interleaved by the compiler.
-    auto run_chunk = [&](auto nt_const) {
+    // independent dequant/MMA chains can be interleaved by the compiler.  FULL
+    // chunks (every token of every tile valid) carry no masking code at all.
+    auto run_chunk = [&](auto nt_const, auto full_const) {
       constexpr int NT = decltype(nt_const)::value;
+      constexpr bool FULL = decltype(full_const)::value;
       // ---- logits of the chunk's tiles ----
       float sc[NT][4];
       int nvalid[NT];
@@ -589,8 +591,8 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
           sc[tt][2] *= rs1;
           sc[tt][3] *= rs1;
         }
-        nvalid[tt] = min(kTile, T - (t0 + c * TPS + tt) * kTile);
-        if (nvalid[tt] < kTile) {
+        nvalid[tt] = FULL ? kTile : min(kTile, T - (t0 + c * TPS + tt) * kTile);
+        if (!FULL && nvalid[tt] < kTile) {
           if (r >= nvalid[tt]) sc[tt][0] = sc[tt][1] = -INFINITY;
           if (r + 8 >= nvalid[tt]) sc[tt][2] = sc[tt][3] = -INFINITY;
         }
@@ -634,16 +636,19 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         l0 += p0 + p2;
         l1 += p1 + p3;
         const uint8_t* tb = stage + tt * Tr::kTileBytes;
-        tile_pv<F>(tb + Tr::kData, tb + 2 * Tr::kData + Tr::kScale, r, q, nvalid[tt], p0, p1, p2, p3,
-                   o, vref);
+        tile_pv<F>(tb + Tr::kData, tb + 2 * Tr::kData + Tr::kScale, r, q, FULL ? kTile : nvalid[tt], p0,
+                   p1, p2, p3, o, vref);
       }
     };
-    if (ntc == TPS) {
-      run_chunk(std::integral_constant<int, TPS>{});
+    using False_ = std::false_type;
+    if (ntc == TPS && (t0 + c * TPS + TPS) * kTile <= T) {
+      run_chunk(std::integral_constant<int, TPS>{}, std::true_type{});
+    } else if (ntc == TPS) {
+      run_chunk(std::integral_constant<int, TPS>{}, False_{});
     } else if (ntc == 1) {
-      run_chunk(std::integral_constant<int, 1>{});
+      run_chunk(std::integral_constant<int, 1>{}, False_{});
     } else {
-      if constexpr (TPS >= 3) run_chunk(std::integral_constant<int, 2>{});  // 2-tile tail of a 3-tile stage
+      if constexpr (TPS >= 3) run_chunk(std::integral_constant<int, 2>{}, False_{});  // 2-tile tail of a 3-tile stage
     }
     static_assert(TPS <= 3, "chunk tails above 2 tiles need their own case");
 
