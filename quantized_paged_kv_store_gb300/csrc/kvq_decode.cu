@@ -519,31 +519,39 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
              (my_kind == 0 ? 0u : my_kind == 1 ? (uint32_t)Tr::kData
                                  : my_kind == 2 ? 2u * Tr::kData : 2u * Tr::kData + Tr::kScale);
   }
-  int sub = t0 % tiles_per_page;  // tile index within its page of the next chunk's first tile
+  // Per lane: tile (of the sequence) that this lane's copy fetches in the next
+  // chunk issued, and the offset of that chunk's first tile in the page-id
+  // window; both advance by TPS per chunk (kPidWin is a multiple of TPS).
+  int ktile = t0 + my_tile;
+  int koff = 0, win = 0;
+  const int tpp_mask = (tiles_per_page & (tiles_per_page - 1)) == 0 ? tiles_per_page - 1 : -1;
+  const uint32_t npages = (uint32_t)min(a.num_pages, (long long)0x7FFFFFFF);
+  const uint32_t page_stride = (uint32_t)my_page_stride;  // < 2^31 (checked at plan time)
 
   // issue chunk c (tiles c*TPS ..) into stage issued % S; all lanes call
   auto issue = [&](int c) {
-    const int k0 = c * TPS;
-    const int ntc = min(TPS, n - k0);
-    if (k0 > 0 && (k0 % kPidWin) == 0) {
+    const int ntc = min(TPS, n - c * TPS);
+    if (koff == kPidWin) {  // the next window of page ids
+      koff = 0;
+      ++win;
       pid_cur = pid_next;
-      pid_next = load_pid(k0 / kPidWin + 1);
+      pid_next = load_pid(win + 1);
     }
-    const int page = __shfl_sync(0xffffffffu, pid_cur, (k0 + my_tile) % kPidWin);
+    const int page = __shfl_sync(0xffffffffu, pid_cur, koff + my_tile);
     const uint32_t st = ring.issued % S;
     const uint32_t bar = ring.bar + 8 * st;
     const bool mine = copier && my_tile < ntc;
-    const bool ok = __all_sync(0xffffffffu, !mine || (page >= 0 && page < a.num_pages));
+    const bool ok = __all_sync(0xffffffffu, !mine || (uint32_t)page < npages);
     bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
     if (lane == 0) mbar_arrive_tx(bar, ok ? ntc * Tr::kTileBytes : 0);
     if (ok && mine) {
-      int sb = sub + my_tile;  // my_tile < TPS <= 3: at most two wraps
-      while (sb >= tiles_per_page) sb -= tiles_per_page;
+      const int sb = tpp_mask >= 0 ? (ktile & tpp_mask) : (ktile % tiles_per_page);
       bulk_g2s(ring.smem + st * Tr::kStage + my_dst,
-               my_base + (long long)page * my_page_stride + (long long)sb * my_tile_stride, my_bytes, bar);
+               my_base + (uint64_t)(uint32_t)page * page_stride + (uint32_t)(sb * my_tile_stride), my_bytes,
+               bar);
     }
-    sub += ntc;
-    while (sub >= tiles_per_page) sub -= tiles_per_page;
+    koff += TPS;
+    ktile += TPS;
     ring.issued++;
   };
 
@@ -850,6 +858,10 @@ bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_pe
   if (g.head_dim != kHeadDim) { *why = "decode attention supports head_dim == 128 only"; return false; }
   if (g.page_size % kTile != 0) { *why = "decode attention needs page_size % 16 == 0"; return false; }
   if (num_q_heads % g.kv_heads != 0) { *why = "num_q_heads must be a multiple of kv_heads"; return false; }
+  if ((int64_t)g.kv_heads * g.page_size * 2 * g.head_dim >= (int64_t(1) << 31)) {
+    *why = "decode attention needs kv_heads * page_size * row bytes < 2^31";
+    return false;
+  }
   const int G = num_q_heads / g.kv_heads;
   if (G > 2 * kGroupMax) { *why = "group size num_q_heads / kv_heads must be <= 16"; return false; }
   int sms = 0, per_sm = 0;
