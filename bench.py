@@ -43,9 +43,9 @@ DTYPE = {"bf16": "bf16 cache; bf16 mma, f32 accumulate",
          "fp4_mx_block16": "e2m1+e8m0 cache; f16 mma, f32 accumulate",
          "nvfp4": "e2m1+e4m3 cache; f16 mma, f32 accumulate"}
 # dram read+write bytes per decode call on the full-size workload, from an ncu
-# capture of the batch-8 case scaled by units processed (profiles/
-# decode_nvfp4_70b_32kx32.md), keyed by the hash of the split-kernel sources it
-# was taken on: any change to those sources reports null until re-measured.
+# capture of the batch-8 case of the same workload scaled by units processed,
+# keyed by the hash of the split-kernel sources it was taken on: any change to
+# those sources reports null until re-measured.
 NCU_TRAFFIC = {("nvfp4", "5acf02030e289748"): 1089900000}
 
 
