@@ -71,6 +71,8 @@ def _load():
             lib.orc_decode_attention.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp,
                                                  i32, vp, i32, vp, i32, vp, i32, f64, vp]
             lib.orc_decode_attention.restype = i32
+            lib.orc_calibrate_scales.argtypes = [i32, i32, i32, vp, i32, i32, vp]
+            lib.orc_calibrate_scales.restype = i32
             lib.orc_num_threads.argtypes = []
             lib.orc_num_threads.restype = i32
             _lib = lib
@@ -131,6 +133,16 @@ def num_threads() -> int:
     return _load().orc_num_threads()
 
 
+def calibrate_scales(fmt, x_bf16: np.ndarray, per_head: bool) -> np.ndarray:
+    """Scale(s) of a format from a batch of bf16 rows x [n][H][D] (reading R16):
+    float32 [H] per kv head, or [1] per tensor."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    n, H, D = x.shape
+    out = np.zeros(H if per_head else 1, np.float32)
+    _load().orc_calibrate_scales(_fmt(fmt), H, D, _ptr(x), n, int(bool(per_head)), _ptr(out))
+    return out
+
+
 # --- cache model ------------------------------------------------------------
 
 def data_row_bytes(fmt, head_dim: int) -> int:
@@ -150,7 +162,14 @@ class OracleCache:
         self.v_data = np.zeros((rows, rb), np.uint8)
         self.k_scales = np.zeros((rows, head_dim // 16), np.uint8)
         self.v_scales = np.zeros((rows, head_dim // 16), np.uint8)
-        self.scales = np.ones(2, np.float32)
+        self.scales = np.ones((2, kv_heads), np.float32)   # [K|V][kv head] (reading R15)
+
+    def set_scales(self, scales) -> None:
+        """{k, v} per tensor, or a [2][H] array of per-kv-head scales."""
+        a = np.asarray(scales, np.float32)
+        if a.shape == (2,):   # per tensor: every head takes the tensor's scale
+            a = np.repeat(a.reshape(2, 1), self.H, axis=1)
+        self.scales = np.ascontiguousarray(a.reshape(2, self.H), dtype=np.float32).copy()
 
     def quantize_store(self, k_bf16: np.ndarray, v_bf16: np.ndarray, slots: np.ndarray,
                        scales=None) -> int:
@@ -159,7 +178,7 @@ class OracleCache:
         v = np.ascontiguousarray(v_bf16, dtype=np.uint16)
         s = np.ascontiguousarray(slots, dtype=np.int64)
         if scales is not None:
-            self.scales = np.asarray(scales, np.float32).copy()
+            self.set_scales(scales)
         n = s.shape[0]
         assert k.shape == (n, self.H, self.D) and v.shape == k.shape
         return _load().orc_quantize_store(self.fmt, self.H, self.D, self.P, self.num_pages,

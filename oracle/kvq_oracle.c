@@ -15,6 +15,8 @@
  *           INT8, FP8, INT4: measured numbers; When to enable.
  *   [NVFP4] "SGLang PR #21954 analysis: NVFP4 KV cache" (secrett2633 blog):
  *           Code analysis 1 (fp4_kv_cache_quant_method.py), Review feedback.
+ *   [VLLM-KV] "Quantized KV cache" (vLLM features page on the data-sketchers
+ *           wiki): Supported schemes; Scale calibration approaches.
  *   The formats themselves are the OCP 8-bit floating point (OFP8) and OCP
  *   Microscaling (MX) v1.0 definitions that [QKV] names.
  *
@@ -40,6 +42,15 @@
  *   R8  Dequantize: out = bf16_RNE(fp32(dec(code) * S)).
  *   R9  Attention: q head j reads kv head floor(j / G), G = Hq / Hkv; a
  *       sequence of length 0 gives an all-zero output.
+ *   R15 Per-attention-head scales ([VLLM-KV] Supported schemes): the FP8
+ *       scale (and the NVFP4 global scale) of kv head h is scales[h] of K or
+ *       V; per-tensor scales are the case where every head has the same one.
+ *   R16 Calibration from a batch of K or V rows ([VLLM-KV] Scale calibration
+ *       approaches, random-token mode; [QKV] Scaling factors): amax over the
+ *       finite values (per tensor, or per kv head); scale = amax / M in fp32
+ *       with M = 448 (E4M3), 57344 (E5M2), 6 * 448 = 2688 (NVFP4 global scale,
+ *       so the largest block scale lands on the E4M3 maximum); amax == 0
+ *       gives 1.0, the pages' default scale.
  *   Non-finite K/V values are outside the contract for the FP4 formats.
  *
  * Parity pins: R4 and R5 are this library's own definitions; the pages give
@@ -223,12 +234,13 @@ int64_t orc_bytes_per_token(int fmt, int layers, int kv_heads, int head_dim) {
 
 /*
  * k, v: bf16 bits [num_tokens][H][D].  slots[i] = page * P + offset, or -1
- * to skip token i.  scales: FP8 {k_scale, v_scale}; NVFP4 {g_k, g_v};
- * otherwise ignored.  Writes the data rows and (block formats) scale rows.
+ * to skip token i.  scales: [2][H] (K heads, then V heads): FP8 scales or
+ * NVFP4 global scales per kv head (R15), NULL for 1.0; ignored by bf16 and
+ * FP4 block-16.  Writes the data rows and (block formats) scale rows.
  * Returns 0, or -1 if a slot is out of range (that token is skipped).
  */
 static int store_one(int fmt, int H, int D, int P, int64_t num_pages, const uint16_t* x,
-                     const int64_t* slots, int num_tokens, float s, uint8_t* data,
+                     const int64_t* slots, int num_tokens, const float* sh, uint8_t* data,
                      uint8_t* scl) {
   int bad = 0;
   size_t drow = data_row_bytes(fmt, D), srow = (size_t)D / 16;
@@ -241,6 +253,7 @@ static int store_one(int fmt, int H, int D, int P, int64_t num_pages, const uint
     if (slot >= num_pages * P) { bad = 1; continue; }
     int64_t page = slot / P, off = slot % P;
     for (int h = 0; h < H; ++h) {
+      const float s = sh[h];                             /* R15: scale of kv head h */
       const uint16_t* row = x + ((size_t)i * H + h) * D;
       size_t r = ((size_t)page * H + h) * P + (size_t)off;
       uint8_t* out = data + r * drow;
@@ -297,18 +310,49 @@ static int store_one(int fmt, int H, int D, int P, int64_t num_pages, const uint
   return bad ? -1 : 0;
 }
 
+/* H ones (the scales when none are given); caller frees */
+static float* ones_for(int H) {
+  float* o = (float*)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+  for (int h = 0; h < H; ++h) o[h] = 1.0f;
+  return o;
+}
+
 int orc_quantize_store(int fmt, int H, int D, int P, int64_t num_pages, const uint16_t* k,
                        const uint16_t* v, const int64_t* slots, int num_tokens,
                        const float* scales, uint8_t* k_data, uint8_t* v_data, uint8_t* k_scl,
                        uint8_t* v_scl) {
-  float sk = scales ? scales[0] : 1.0f, sv = scales ? scales[1] : 1.0f;
+  float* ones;
   int rk, rv;
   if (D % 16 != 0 || fmt < 0 || fmt > 4) return -2;
-  rk = store_one(fmt, H, D, P, num_pages, k, slots, num_tokens, sk, k_data,
-                 has_block_scales(fmt) ? k_scl : NULL);
-  rv = store_one(fmt, H, D, P, num_pages, v, slots, num_tokens, sv, v_data,
-                 has_block_scales(fmt) ? v_scl : NULL);
+  ones = scales ? NULL : ones_for(H);
+  rk = store_one(fmt, H, D, P, num_pages, k, slots, num_tokens, scales ? scales : ones,
+                 k_data, has_block_scales(fmt) ? k_scl : NULL);
+  rv = store_one(fmt, H, D, P, num_pages, v, slots, num_tokens, scales ? scales + H : ones,
+                 v_data, has_block_scales(fmt) ? v_scl : NULL);
+  free(ones);
   return (rk || rv) ? -1 : 0;
+}
+
+/* Calibration (R16): scale(s) from the amax of x [n][H][D] (bf16 bits) over
+ * the finite values, per kv head (out[0..H-1]) or per tensor (out[0]). */
+int orc_calibrate_scales(int fmt, int H, int D, const uint16_t* x, int n, int per_head,
+                         float* out) {
+  float M;
+  if (fmt == ORC_E4M3) M = 448.0f;
+  else if (fmt == ORC_E5M2) M = 57344.0f;
+  else if (fmt == ORC_NVFP4) M = 6.0f * 448.0f;
+  else M = 0.0f;                                     /* no per-tensor scale: 1.0 */
+  for (int h = 0; h < (per_head ? H : 1); ++h) out[h] = 0.0f;
+  for (int i = 0; i < n; ++i)
+    for (int h = 0; h < H; ++h)
+      for (int d = 0; d < D; ++d) {
+        float a = fabsf(bf16_to_float(x[((size_t)i * H + h) * D + d]));
+        float* o = &out[per_head ? h : 0];
+        if (isfinite(a) && a > *o) *o = a;
+      }
+  for (int h = 0; h < (per_head ? H : 1); ++h)
+    out[h] = (M > 0.0f && out[h] > 0.0f) ? out[h] / M : 1.0f;   /* fp32 division */
+  return 0;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -340,7 +384,8 @@ static float element_scale_f32(int fmt, const uint8_t* srow, int d, float s) {
 
 /* out = bf16_RNE(fp32(dec(code) * S)); slots < 0 give a zero row. */
 static int dequant_one(int fmt, int H, int D, int P, int64_t num_pages, const uint8_t* data,
-                       const uint8_t* scl, const int64_t* slots, int n, float s, uint16_t* out) {
+                       const uint8_t* scl, const int64_t* slots, int n, const float* sh,
+                       uint16_t* out) {
   int bad = 0;
   size_t drow = data_row_bytes(fmt, D), srow = (size_t)D / 16;
   for (int i = 0; i < n; ++i) {
@@ -348,6 +393,7 @@ static int dequant_one(int fmt, int H, int D, int P, int64_t num_pages, const ui
     int valid = slot >= 0 && slot < num_pages * P;
     if (slot >= 0 && !valid) bad = 1;
     for (int h = 0; h < H; ++h) {
+      const float s = sh[h];
       uint16_t* o = out + ((size_t)i * H + h) * D;
       if (!valid) { memset(o, 0, (size_t)D * 2); continue; }
       size_t r = ((size_t)(slot / P) * H + h) * P + (size_t)(slot % P);
@@ -374,10 +420,13 @@ int orc_dequantize(int fmt, int H, int D, int P, int64_t num_pages, const uint8_
                    const uint8_t* v_data, const uint8_t* k_scl, const uint8_t* v_scl,
                    const float* scales, const int64_t* slots, int n, uint16_t* k_out,
                    uint16_t* v_out) {
-  float sk = scales ? scales[0] : 1.0f, sv = scales ? scales[1] : 1.0f;
+  float* ones = scales ? NULL : ones_for(H);
   int bs = has_block_scales(fmt);
-  int rk = dequant_one(fmt, H, D, P, num_pages, k_data, bs ? k_scl : NULL, slots, n, sk, k_out);
-  int rv = dequant_one(fmt, H, D, P, num_pages, v_data, bs ? v_scl : NULL, slots, n, sv, v_out);
+  int rk = dequant_one(fmt, H, D, P, num_pages, k_data, bs ? k_scl : NULL, slots, n,
+                       scales ? scales : ones, k_out);
+  int rv = dequant_one(fmt, H, D, P, num_pages, v_data, bs ? v_scl : NULL, slots, n,
+                       scales ? scales + H : ones, v_out);
+  free(ones);
   return (rk || rv) ? -1 : 0;
 }
 
@@ -391,7 +440,8 @@ int orc_dequantize(int fmt, int H, int D, int P, int64_t num_pages, const uint8_
  * For every b in b_list (or every b when b_list is NULL) and every q head j:
  *   z_t = sm_scale * sum_d q[b][j][d] * K^[t][d],  t < seq_lens[b]
  *   out[b][j][:] = sum_t softmax(z)_t * V^[t][:]
- * with K^, V^ the exact dequantized values.  Output rows of sequences not in
+ * with K^, V^ the exact dequantized values (scales [2][H] as for the store).
+ * Output rows of sequences not in
  * b_list are left untouched.  Returns 0, or -1 if a page id is out of range
  * (the affected rows are set to zero).
  */
@@ -400,7 +450,6 @@ int orc_decode_attention(int fmt, int H, int D, int P, int64_t num_pages, const 
                          const float* scales, const uint16_t* q, int Hq,
                          const int32_t* page_table, int max_pages, const int32_t* seq_lens,
                          int B, const int32_t* b_list, int nb, double sm_scale, double* out) {
-  float sk = scales ? scales[0] : 1.0f, sv = scales ? scales[1] : 1.0f;
   int G, bad = 0;
   int nsel = b_list ? nb : B;
   size_t drow = data_row_bytes(fmt, D), srow = (size_t)D / 16;
@@ -412,6 +461,7 @@ int orc_decode_attention(int fmt, int H, int D, int P, int64_t num_pages, const 
   for (int64_t w = 0; w < (int64_t)nsel * H; ++w) {
     int b = b_list ? b_list[w / H] : (int)(w / H);
     int h = (int)(w % H);
+    const float sk = scales ? scales[h] : 1.0f, sv = scales ? scales[H + h] : 1.0f;  /* R15 */
     int T = seq_lens[b];
     double* z = NULL;
     double* kv = (double*)malloc(sizeof(double) * (size_t)D);
