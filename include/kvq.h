@@ -125,6 +125,46 @@ kvq_status kvq_quantize_and_store(kvq_cache* cache, int layer, const void* k_bf1
                                   int num_tokens, const float* scales, kvq_stream stream);
 
 /*
+ * kvq_quantize_and_store with one scale per kv head ([VLLM] Supported
+ * schemes: per-attention-head quantization, k/v_scale = [num_kv_heads]).
+ *   k_scales, v_scales (host): [kv_heads] floats, finite and > 0 -- the FP8
+ *                   scales or the NVFP4 global scales of each kv head; ignored
+ *                   (may be NULL) for bf16 and fp4_mx_block16.
+ * Every kv head h is quantized as with kvq_quantize_and_store and scale
+ * k_scales[h] / v_scales[h]; attention and kvq_dequantize use the same scale
+ * per head.  Equal scales on every head are exactly the per-tensor case.  The
+ * first store of a layer that stores tokens fixes its scales (with either
+ * entry point, or kvq_calibrate_scales); a later store whose scales differ on
+ * any head returns KVQ_ERR_SCALE_MISMATCH.  Other errors as for
+ * kvq_quantize_and_store.
+ */
+kvq_status kvq_quantize_and_store_per_head(kvq_cache* cache, int layer, const void* k_bf16,
+                                           const void* v_bf16, const int64_t* slot_mapping,
+                                           int num_tokens, const float* k_scales,
+                                           const float* v_scales, kvq_stream stream);
+
+/*
+ * Fix the scales of `layer` from a batch of bf16 K and V rows on the device
+ * ([VLLM] Scale calibration approaches: scales estimated on the fly from one
+ * batch of tokens, then fixed; [QKV] Scaling factors).
+ *   k_bf16, v_bf16: [num_tokens][kv_heads][head_dim] bf16 device rows, 16-byte
+ *                   aligned, num_tokens >= 1.
+ *   per_head:       0: one scale per tensor (K and V each); 1: one per kv head.
+ * scale = amax / M over the finite values (per tensor or per kv head), fp32
+ * division, M = 448 (E4M3), 57344 (E5M2), 6 * 448 = 2688 (NVFP4 global scale:
+ * the largest block scale lands on the E4M3 maximum); amax == 0 gives 1.0.
+ * Stream-ordered, no host synchronization, no allocation.  Only valid on a
+ * layer whose scales are not fixed yet (else KVQ_ERR_SCALE_MISMATCH); for bf16
+ * and fp4_mx_block16 it fixes nothing but marks the layer as set.  Later
+ * stores of the layer pass scales == NULL to kvq_quantize_and_store (explicit
+ * scales return KVQ_ERR_SCALE_MISMATCH: the host does not see the values).
+ * Errors: INVALID_ARG, SCALE_MISMATCH, CUDA.
+ */
+kvq_status kvq_calibrate_scales(kvq_cache* cache, int layer, const void* k_bf16,
+                                const void* v_bf16, int num_tokens, int per_head,
+                                kvq_stream stream);
+
+/*
  * Decode attention of one query token per sequence over the cache of
  * `layer`, dequantizing in registers ([QKV] Performance warning; [NVFP4]
  * XQA decode path, here fused).  For sequence b and q head j, with
@@ -203,9 +243,18 @@ kvq_status kvq_dequantize(kvq_cache* cache, int layer, const int64_t* slot_mappi
 kvq_status kvq_cache_layout(const kvq_cache* cache, int layer, void** k_data, void** v_data,
                             void** k_scales, void** v_scales, size_t strides[4]);
 
-/* The scales fixed for `layer` by its first store (host out[2]); returns
- * KVQ_ERR_INVALID_ARG if the layer has not been stored to yet. */
+/* The per-tensor scales fixed for `layer` (host out[2] = {K, V}); returns
+ * KVQ_ERR_INVALID_ARG if the layer has no scales yet or its kv heads have
+ * different scales (read those with kvq_layer_head_scales).  For a calibrated
+ * layer it synchronizes the device first. */
 kvq_status kvq_layer_scales(const kvq_cache* cache, int layer, float out[2]);
+
+/* The per-kv-head scales of a layer (k_out, v_out: host [kv_heads] each):
+ * the values its first store fixed, or, for a calibrated layer, the values
+ * the device computed (this synchronizes `stream` first).  INVALID_ARG if the
+ * layer has no scales yet. */
+kvq_status kvq_layer_head_scales(const kvq_cache* cache, int layer, float* k_out, float* v_out,
+                                 kvq_stream stream);
 
 /* Cache bytes per token for a model: 2 (K, V) x layers x kv_heads x bytes per
  * head row, including one scale byte per 16 elements for the FP4 formats

@@ -30,6 +30,9 @@ def _load():
         "kvq_create_cache": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(vp)], i32),
         "kvq_destroy_cache": ([vp], i32),
         "kvq_quantize_and_store": ([vp, i32, vp, vp, vp, i32, vp, vp], i32),
+        "kvq_quantize_and_store_per_head": ([vp, i32, vp, vp, vp, i32, vp, vp, vp], i32),
+        "kvq_calibrate_scales": ([vp, i32, vp, vp, i32, i32, vp], i32),
+        "kvq_layer_head_scales": ([vp, i32, ctypes.POINTER(f32), ctypes.POINTER(f32), vp], i32),
         "kvq_decode_attention": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp, sz, vp], i32),
         "kvq_decode_workspace_size": ([vp, i32, i32, i32], sz),
         "kvq_decode_attention_noalloc": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp], i32),
@@ -118,6 +121,32 @@ def kvq_quantize_and_store(handle, layer, k, v, slot_mapping, scales=None, strea
                                       _stream(stream)), "kvq_quantize_and_store")
 
 
+def kvq_quantize_and_store_per_head(handle, layer, k, v, slot_mapping, k_scales, v_scales,
+                                    stream=None):
+    """As kvq_quantize_and_store with host sequences of one scale per kv head."""
+    def arr(x):
+        return None if x is None else (ctypes.c_float * len(x))(*[float(t) for t in x])
+    _check(lib.kvq_quantize_and_store_per_head(ctypes.c_void_p(handle), layer, _ptr(k), _ptr(v),
+                                               _ptr(slot_mapping), int(slot_mapping.shape[0]),
+                                               arr(k_scales), arr(v_scales), _stream(stream)),
+           "kvq_quantize_and_store_per_head")
+
+
+def kvq_calibrate_scales(handle, layer, k, v, per_head: bool, stream=None):
+    """Fixes the layer's scales from bf16 K, V device rows [n][kv_heads][head_dim]."""
+    _check(lib.kvq_calibrate_scales(ctypes.c_void_p(handle), layer, _ptr(k), _ptr(v),
+                                    int(k.shape[0]), int(bool(per_head)), _stream(stream)),
+           "kvq_calibrate_scales")
+
+
+def kvq_layer_head_scales(handle, layer, kv_heads, stream=None):
+    ks = (ctypes.c_float * kv_heads)()
+    vs = (ctypes.c_float * kv_heads)()
+    _check(lib.kvq_layer_head_scales(ctypes.c_void_p(handle), layer, ks, vs, _stream(stream)),
+           "kvq_layer_head_scales")
+    return [float(x) for x in ks], [float(x) for x in vs]
+
+
 def kvq_decode_workspace_size(handle, batch, num_q_heads, max_pages_per_seq) -> int:
     n = lib.kvq_decode_workspace_size(ctypes.c_void_p(handle), batch, num_q_heads, max_pages_per_seq)
     if n == 0:
@@ -196,6 +225,17 @@ class KVQCache:
 
     def quantize_and_store(self, layer, k, v, slot_mapping, scales=None, stream=None):
         kvq_quantize_and_store(self.handle, layer, k, v, slot_mapping, scales, stream)
+
+    def quantize_and_store_per_head(self, layer, k, v, slot_mapping, k_scales, v_scales,
+                                    stream=None):
+        kvq_quantize_and_store_per_head(self.handle, layer, k, v, slot_mapping, k_scales, v_scales,
+                                        stream)
+
+    def calibrate_scales(self, layer, k, v, per_head=False, stream=None):
+        kvq_calibrate_scales(self.handle, layer, k, v, per_head, stream)
+
+    def layer_head_scales(self, layer, stream=None):
+        return kvq_layer_head_scales(self.handle, layer, self.kv_heads, stream)
 
     def workspace_size(self, batch, num_q_heads, max_pages_per_seq):
         return kvq_decode_workspace_size(self.handle, batch, num_q_heads, max_pages_per_seq)

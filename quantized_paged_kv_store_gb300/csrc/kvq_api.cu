@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -24,8 +25,14 @@ struct kvq_cache {
   size_t layer_data_bytes; // one K (or V) data pool of one layer
   size_t layer_scale_bytes;
   int* err;                // device error word
-  std::vector<float> scales;    // [layers][2]
-  std::vector<char> scales_set; // [layers]
+  // Scales of each layer ("Quantized KV cache" (vLLM): per-tensor or
+  // per-attention-head; fixed by the first store or by calibration).
+  std::vector<float> scales;    // [layers][2][kv_heads] host copy (mode kHost)
+  std::vector<char> mode;       // [layers] kUnset / kHost / kDevice
+  std::vector<char> uniform;    // [layers] every head has the same scales (mode kHost)
+  float* dscale;                // [layers][2][kv_heads] device copy
+  float* drecip;                // [layers][2][kv_heads] 1 / scale
+  unsigned* damax;              // [2][kv_heads] calibration scratch
 };
 
 namespace {
@@ -80,6 +87,123 @@ kvq_status check_layer(const kvq_cache* c, int layer) {
 }
 
 bool uses_scales(kvq_format f) { return f == KVQ_FP8_E4M3 || f == KVQ_FP8_E5M2 || f == KVQ_NVFP4; }
+
+enum : char { kUnset = 0, kHost = 1, kDevice = 2 };
+
+float* host_scales(kvq_cache* c, int layer, int kv) {
+  return c->scales.data() + ((size_t)layer * 2 + kv) * c->geo.kv_heads;
+}
+const float* host_scales(const kvq_cache* c, int layer, int kv) {
+  return c->scales.data() + ((size_t)layer * 2 + kv) * c->geo.kv_heads;
+}
+
+// Device per-head scales of a layer when its heads differ or were calibrated
+// on the device; null pointers (the per-tensor path) otherwise.
+kvq::HeadScales head_scales(const kvq_cache* c, int layer) {
+  kvq::HeadScales hs;
+  const bool ph = uses_scales(c->geo.fmt) &&
+                  (c->mode[layer] == kDevice || (c->mode[layer] == kHost && !c->uniform[layer]));
+  if (ph) {
+    const size_t H = (size_t)c->geo.kv_heads, base = (size_t)layer * 2 * H;
+    hs.scale[0] = c->dscale + base;
+    hs.scale[1] = c->dscale + base + H;
+    hs.recip[0] = c->drecip + base;
+    hs.recip[1] = c->drecip + base + H;
+  }
+  return hs;
+}
+
+// Per-tensor scales of a layer for the scalar path (1.0 where none apply).
+void tensor_scales(const kvq_cache* c, int layer, float* sk, float* sv) {
+  *sk = *sv = 1.0f;
+  if (uses_scales(c->geo.fmt) && c->mode[layer] == kHost) {
+    *sk = host_scales(c, layer, 0)[0];
+    *sv = host_scales(c, layer, 1)[0];
+  }
+}
+
+kvq_status check_scale_values(const float* s, int n) {
+  for (int i = 0; i < n; ++i)
+    if (!std::isfinite(s[i]) || !(s[i] > 0.0f))
+      return fail(KVQ_ERR_INVALID_ARG, "scales must be finite and > 0 (got %g)", (double)s[i]);
+  return KVQ_OK;
+}
+
+kvq_status check_rows(const kvq_cache* c, const void* k, const void* v) {
+  if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+  if (!aligned16(k) || !aligned16(v)) return fail(KVQ_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  return check_device(c);
+}
+
+// Fixes a layer's scales from host values (k[H], v[H]) on its first store that
+// stores tokens (fix), or checks them against the fixed ones.
+kvq_status fix_or_check_scales(kvq_cache* c, int layer, const float* k, const float* v, bool fix,
+                               cudaStream_t stream) {
+  const int H = c->geo.kv_heads;
+  if (c->mode[layer] == kUnset && !fix) return KVQ_OK;
+  if (!uses_scales(c->geo.fmt)) {
+    if (c->mode[layer] == kUnset) {
+      c->mode[layer] = kHost;
+      c->uniform[layer] = 1;
+    }
+    return KVQ_OK;
+  }
+  if (c->mode[layer] == kDevice)
+    return fail(KVQ_ERR_SCALE_MISMATCH,
+                "layer %d scales were calibrated on the device; store it with NULL scales", layer);
+  if (c->mode[layer] == kHost) {
+    for (int h = 0; h < H; ++h)
+      if (host_scales(c, layer, 0)[h] != k[h] || host_scales(c, layer, 1)[h] != v[h])
+        return fail(KVQ_ERR_SCALE_MISMATCH,
+                    "layer %d scales are fixed (kv head %d: {%g, %g}); got {%g, %g}", layer, h,
+                    (double)host_scales(c, layer, 0)[h], (double)host_scales(c, layer, 1)[h],
+                    (double)k[h], (double)v[h]);
+    return KVQ_OK;
+  }
+  bool uni = true;
+  for (int h = 0; h < H; ++h) {
+    host_scales(c, layer, 0)[h] = k[h];
+    host_scales(c, layer, 1)[h] = v[h];
+    uni = uni && k[h] == k[0] && v[h] == v[0];
+  }
+  const size_t base = (size_t)layer * 2 * H;
+  cudaError_t e = kvq::launch_set_head_scales(c->dscale + base, c->drecip + base, k, v, H, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "set layer scales");
+  c->mode[layer] = kHost;
+  c->uniform[layer] = uni;
+  return KVQ_OK;
+}
+
+kvq_status store_launch(kvq_cache* c, int layer, const void* k_bf16, const void* v_bf16,
+                        const int64_t* slot_mapping, int num_tokens, cudaStream_t stream) {
+  float sk, sv;
+  tensor_scales(c, layer, &sk, &sv);
+  cudaError_t e = kvq::launch_store(c->geo, view(c, layer), k_bf16, v_bf16, slot_mapping,
+                                    num_tokens, sk, sv, head_scales(c, layer), c->err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize-and-store launch");
+  return KVQ_OK;
+}
+
+// Reads a layer's per-head scales into k_out / v_out ([kv_heads] each).
+kvq_status read_layer_scales(const kvq_cache* c, int layer, float* k_out, float* v_out,
+                             cudaStream_t stream, bool sync_device) {
+  const int H = c->geo.kv_heads;
+  if (c->mode[layer] == kUnset) return fail(KVQ_ERR_INVALID_ARG, "layer %d has no stored data yet", layer);
+  if (c->mode[layer] == kHost) {
+    std::memcpy(k_out, host_scales(c, layer, 0), sizeof(float) * H);
+    std::memcpy(v_out, host_scales(c, layer, 1), sizeof(float) * H);
+    return KVQ_OK;
+  }
+  kvq_status st = check_device(c);
+  if (st) return st;
+  cudaError_t e = sync_device ? cudaDeviceSynchronize() : cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "synchronize before reading calibrated scales");
+  const float* d = c->dscale + (size_t)layer * 2 * H;
+  if ((e = cudaMemcpy(k_out, d, sizeof(float) * H, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(v_out, d + H, sizeof(float) * H, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read calibrated scales");
+  return KVQ_OK;
+}
 
 }  // namespace
 
@@ -145,7 +269,10 @@ kvq_status kvq_create_cache(kvq_format fmt, int layers, int kv_heads, int head_d
   const size_t rows = (size_t)num_pages * kv_heads * page_size;
   const size_t ldb = (rows * g.data_row + 255) & ~(size_t)255;
   const size_t lsb = (rows * g.scale_row + 255) & ~(size_t)255;
-  const size_t total = (2 * ldb + 2 * lsb) * (size_t)layers + 256;
+  const size_t scale_bytes = ((size_t)layers * 2 * kv_heads * sizeof(float) + 255) & ~(size_t)255;
+  const size_t amax_bytes = (2 * (size_t)kv_heads * sizeof(unsigned) + 255) & ~(size_t)255;
+  const size_t pools = (2 * ldb + 2 * lsb) * (size_t)layers;
+  const size_t total = pools + 2 * scale_bytes + amax_bytes + 256;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -179,8 +306,12 @@ kvq_status kvq_create_cache(kvq_format fmt, int layers, int kv_heads, int head_d
   c->layer_data_bytes = ldb;
   c->layer_scale_bytes = lsb;
   c->err = reinterpret_cast<int*>(base + total - 256);
-  c->scales.assign((size_t)layers * 2, 1.0f);
-  c->scales_set.assign((size_t)layers, 0);
+  c->dscale = reinterpret_cast<float*>(base + pools);
+  c->drecip = reinterpret_cast<float*>(base + pools + scale_bytes);
+  c->damax = reinterpret_cast<unsigned*>(base + pools + 2 * scale_bytes);
+  c->scales.assign((size_t)layers * 2 * kv_heads, 1.0f);
+  c->mode.assign((size_t)layers, kUnset);
+  c->uniform.assign((size_t)layers, 1);
   *out = c;
   return KVQ_OK;
 }
@@ -222,10 +353,23 @@ kvq_status kvq_layer_scales(const kvq_cache* c, int layer, float out[2]) {
   kvq_status st = check_layer(c, layer);
   if (st) return st;
   if (!out) return fail(KVQ_ERR_INVALID_ARG, "out is NULL");
-  if (!c->scales_set[layer]) return fail(KVQ_ERR_INVALID_ARG, "layer %d has no stored data yet", layer);
-  out[0] = c->scales[2 * layer];
-  out[1] = c->scales[2 * layer + 1];
+  std::vector<float> k(c->geo.kv_heads), v(c->geo.kv_heads);
+  if ((st = read_layer_scales(c, layer, k.data(), v.data(), nullptr, true))) return st;
+  for (int h = 1; h < c->geo.kv_heads; ++h)
+    if (k[h] != k[0] || v[h] != v[0])
+      return fail(KVQ_ERR_INVALID_ARG,
+                  "layer %d has per-head scales; read them with kvq_layer_head_scales", layer);
+  out[0] = k[0];
+  out[1] = v[0];
   return KVQ_OK;
+}
+
+kvq_status kvq_layer_head_scales(const kvq_cache* c, int layer, float* k_out, float* v_out,
+                                 kvq_stream stream) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  if (!k_out || !v_out) return fail(KVQ_ERR_INVALID_ARG, "NULL output array");
+  return read_layer_scales(c, layer, k_out, v_out, (cudaStream_t)stream, false);
 }
 
 kvq_status kvq_quantize_and_store(kvq_cache* c, int layer, const void* k_bf16, const void* v_bf16,
@@ -234,35 +378,70 @@ kvq_status kvq_quantize_and_store(kvq_cache* c, int layer, const void* k_bf16, c
   kvq_status st = check_layer(c, layer);
   if (st) return st;
   if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "num_tokens < 0");
-  float s[2] = {1.0f, 1.0f};
+  const bool calibrated = c->mode[layer] == kDevice;
+  std::vector<float> k(c->geo.kv_heads, 1.0f), v(c->geo.kv_heads, 1.0f);
   if (uses_scales(c->geo.fmt) && scales) {
-    for (int i = 0; i < 2; ++i) {
-      if (!std::isfinite(scales[i]) || !(scales[i] > 0.0f))
-        return fail(KVQ_ERR_INVALID_ARG, "scales must be finite and > 0 (got %g)", (double)scales[i]);
-      s[i] = scales[i];
-    }
-  }
-  if (c->scales_set[layer]) {
-    if (uses_scales(c->geo.fmt) &&
-        (c->scales[2 * layer] != s[0] || c->scales[2 * layer + 1] != s[1]))
+    if ((st = check_scale_values(scales, 2))) return st;
+    if (calibrated)
       return fail(KVQ_ERR_SCALE_MISMATCH,
-                  "layer %d scales are fixed at {%g, %g}; got {%g, %g}", layer,
-                  (double)c->scales[2 * layer], (double)c->scales[2 * layer + 1], (double)s[0],
-                  (double)s[1]);
+                  "layer %d scales were calibrated on the device; store it with NULL scales", layer);
+    std::fill(k.begin(), k.end(), scales[0]);
+    std::fill(v.begin(), v.end(), scales[1]);
   }
+  if (num_tokens > 0) {
+    if (!slot_mapping) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+    if ((st = check_rows(c, k_bf16, v_bf16))) return st;
+  }
+  if (!calibrated && (st = fix_or_check_scales(c, layer, k.data(), v.data(), num_tokens > 0,
+                                               (cudaStream_t)stream)))
+    return st;
   if (num_tokens == 0) return KVQ_OK;
-  if (!k_bf16 || !v_bf16 || !slot_mapping) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
-  if (!aligned16(k_bf16) || !aligned16(v_bf16))
-    return fail(KVQ_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
-  if ((st = check_device(c))) return st;
-  if (!c->scales_set[layer]) {
-    c->scales[2 * layer] = s[0];
-    c->scales[2 * layer + 1] = s[1];
-    c->scales_set[layer] = 1;
+  return store_launch(c, layer, k_bf16, v_bf16, slot_mapping, num_tokens, (cudaStream_t)stream);
+}
+
+kvq_status kvq_quantize_and_store_per_head(kvq_cache* c, int layer, const void* k_bf16,
+                                           const void* v_bf16, const int64_t* slot_mapping,
+                                           int num_tokens, const float* k_scales,
+                                           const float* v_scales, kvq_stream stream) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "num_tokens < 0");
+  const int H = c->geo.kv_heads;
+  std::vector<float> k(H, 1.0f), v(H, 1.0f);
+  if (uses_scales(c->geo.fmt)) {
+    if (!k_scales || !v_scales) return fail(KVQ_ERR_INVALID_ARG, "per-head scales are NULL");
+    if ((st = check_scale_values(k_scales, H)) || (st = check_scale_values(v_scales, H))) return st;
+    k.assign(k_scales, k_scales + H);
+    v.assign(v_scales, v_scales + H);
   }
-  cudaError_t e = kvq::launch_store(c->geo, view(c, layer), k_bf16, v_bf16, slot_mapping,
-                                    num_tokens, s[0], s[1], c->err, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "quantize-and-store launch");
+  if (num_tokens > 0) {
+    if (!slot_mapping) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+    if ((st = check_rows(c, k_bf16, v_bf16))) return st;
+  }
+  if ((st = fix_or_check_scales(c, layer, k.data(), v.data(), num_tokens > 0, (cudaStream_t)stream)))
+    return st;
+  if (num_tokens == 0) return KVQ_OK;
+  return store_launch(c, layer, k_bf16, v_bf16, slot_mapping, num_tokens, (cudaStream_t)stream);
+}
+
+kvq_status kvq_calibrate_scales(kvq_cache* c, int layer, const void* k_bf16, const void* v_bf16,
+                                int num_tokens, int per_head, kvq_stream stream) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  if (num_tokens <= 0) return fail(KVQ_ERR_INVALID_ARG, "calibration needs num_tokens > 0");
+  if (c->mode[layer] != kUnset)
+    return fail(KVQ_ERR_SCALE_MISMATCH, "layer %d scales are already fixed", layer);
+  if ((st = check_rows(c, k_bf16, v_bf16))) return st;
+  if (!uses_scales(c->geo.fmt)) {  // nothing to calibrate: the layer keeps scale 1.0
+    c->mode[layer] = kHost;
+    c->uniform[layer] = 1;
+    return KVQ_OK;
+  }
+  const size_t base = (size_t)layer * 2 * c->geo.kv_heads;
+  cudaError_t e = kvq::launch_calibrate(c->geo, k_bf16, v_bf16, num_tokens, per_head != 0, c->damax,
+                                        c->dscale + base, c->drecip + base, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "calibration launch");
+  c->mode[layer] = kDevice;
   return KVQ_OK;
 }
 
@@ -276,9 +455,11 @@ kvq_status kvq_dequantize(kvq_cache* c, int layer, const int64_t* slot_mapping, 
   if (!aligned16(k_out_bf16) || !aligned16(v_out_bf16))
     return fail(KVQ_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
   if ((st = check_device(c))) return st;
-  cudaError_t e = kvq::launch_dequantize(c->geo, view(c, layer), slot_mapping, num_tokens,
-                                         c->scales[2 * layer], c->scales[2 * layer + 1], k_out_bf16,
-                                         v_out_bf16, c->err, (cudaStream_t)stream);
+  float sk, sv;
+  tensor_scales(c, layer, &sk, &sv);
+  cudaError_t e = kvq::launch_dequantize(c->geo, view(c, layer), slot_mapping, num_tokens, sk, sv,
+                                         head_scales(c, layer), k_out_bf16, v_out_bf16, c->err,
+                                         (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
   return KVQ_OK;
 }
@@ -318,12 +499,12 @@ kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q_bf16, int
   if (workspace_bytes < plan.ws_bytes)
     return fail(KVQ_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, plan.ws_bytes);
   if ((st = check_device(c))) return st;
-  const kvq_format f = c->geo.fmt;
-  const float kf = uses_scales(f) ? c->scales[2 * layer] : 1.0f;
-  const float vf = uses_scales(f) ? c->scales[2 * layer + 1] : 1.0f;
+  float kf, vf;
+  tensor_scales(c, layer, &kf, &vf);
   cudaError_t e = kvq::launch_decode(c->geo, view(c, layer), plan, q_bf16, num_q_heads, page_table,
-                                     max_pages_per_seq, seq_lens, batch, sm_scale, kf, vf, out_bf16,
-                                     workspace, c->err, (cudaStream_t)stream);
+                                     max_pages_per_seq, seq_lens, batch, sm_scale, kf, vf,
+                                     head_scales(c, layer), out_bf16, workspace, c->err,
+                                     (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   return KVQ_OK;
 }

@@ -475,7 +475,9 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         qb[j][1] = f32x2_to_h2(bf16_bits_to_float(w16[2 * j + 1] & 0xFFFF) * mul,
                                bf16_bits_to_float(w16[2 * j + 1] >> 16) * mul);
       }
-      colscale = (r < gh) ? a.qscale * exp2i(sq) : 1.f;
+      // per-kv-head K scale (one per unit), else the per-tensor one folded on the host
+      const float qs = a.kfac ? a.qscale * __ldg(a.kfac + h) : a.qscale;
+      colscale = (r < gh) ? qs * exp2i(sq) : 1.f;
     }
   }
   // D1 columns of this thread are heads 2q, 2q+1 (held by lanes 8q and 8q+4 above)
@@ -679,7 +681,7 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
   if (poison && lane == 0 && !ring.dead) atomicOr(a.err, kErrRange);
   const long long u = ((long long)b * a.H + h) * a.HG + hg;
   const long long slot = u + w;
-  float vscale = a.v_factor;
+  float vscale = a.vfac ? __ldg(a.vfac + h) : a.v_factor;
   if (F == KVQ_FP4_BLOCK16) vscale *= exp2i(max(-127, min(127, vref - 127)));
   const float inv0 = poison ? 0.f : vscale / l0, inv1 = poison ? 0.f : vscale / l1;
   // thread (r, q): heads 2q, 2q+1; d = 16 r + mt (c0, c1) and 16 r + 8 + mt (c2, c3)
@@ -894,8 +896,8 @@ bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_pe
 cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePlan& plan,
                           const void* q, int num_q_heads, const int32_t* page_table,
                           int max_pages_per_seq, const int32_t* seq_lens, int batch,
-                          float sm_scale, float k_factor, float v_factor, void* out,
-                          void* workspace, int* err, cudaStream_t stream) {
+                          float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
+                          void* out, void* workspace, int* err, cudaStream_t stream) {
   DecodeArgs a;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.part_o = reinterpret_cast<float*>(ws);
@@ -922,7 +924,10 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
   a.P = g.page_size;
   a.num_pages = g.num_pages;
   a.num_workers = plan.num_workers;
-  a.qscale = sm_scale * 1.4426950408889634f * k_factor;
+  // per-head scales multiply in the kernel, after the same sm_scale * log2(e)
+  a.kfac = hs.scale[0];
+  a.vfac = hs.scale[1];
+  a.qscale = sm_scale * 1.4426950408889634f * (a.kfac ? 1.0f : k_factor);
   a.v_factor = v_factor;
   a.err = err;
   if (batch == 0) return cudaSuccess;

@@ -26,9 +26,11 @@ struct DecodeArgs {
   int B, H, Hq, G, HG, max_pages, P;
   long long num_pages;
   int num_workers;
-  float qscale;       // sm_scale * log2(e) * (k_scale | g_k | 1)
-  float v_factor;     // v_scale | g_v | 1
+  float qscale;       // sm_scale * log2(e) * (k_scale | g_k | 1); without the factor if kfac
+  float v_factor;     // v_scale | g_v | 1 (per tensor)
   int* err;
+  const float* kfac;  // per-kv-head K scales (or null: per tensor)
+  const float* vfac;  // per-kv-head V scales (or null)
 };
 
 

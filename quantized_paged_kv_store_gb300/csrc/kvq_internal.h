@@ -44,15 +44,36 @@ inline bool has_block_scales(kvq_format f) { return f == KVQ_FP4_BLOCK16 || f ==
 // Sets the thread-local message returned by kvq_last_error_string().
 void set_error_message(const char* fmt, ...);
 
+// Per-kv-head scales of one layer in device memory: scale[0] / scale[1] are
+// the K / V scales ([kv_heads] floats each), recip the IEEE reciprocals.
+// Null pointers select the per-tensor path (scalar scales in the launch).
+struct HeadScales {
+  const float* scale[2] = {nullptr, nullptr};
+  const float* recip[2] = {nullptr, nullptr};
+};
+
 // ---- launchers (defined in the .cu files; return a CUDA error code) -------
 
 cudaError_t launch_store(const Geometry& g, const LayerView& L, const void* k, const void* v,
-                         const int64_t* slots, int num_tokens, float s_k, float s_v, int* err,
-                         cudaStream_t stream);
+                         const int64_t* slots, int num_tokens, float s_k, float s_v,
+                         const HeadScales& hs, int* err, cudaStream_t stream);
 
 cudaError_t launch_dequantize(const Geometry& g, const LayerView& L, const int64_t* slots,
-                              int num_tokens, float s_k, float s_v, void* k_out, void* v_out,
-                              int* err, cudaStream_t stream);
+                              int num_tokens, float s_k, float s_v, const HeadScales& hs,
+                              void* k_out, void* v_out, int* err, cudaStream_t stream);
+
+// Writes host-given per-head scales (k[H], v[H]) and their reciprocals into
+// scale / recip ([2][H] each) with kernel launches on `stream` (the values
+// travel as launch arguments, so the call is capturable in a CUDA graph).
+cudaError_t launch_set_head_scales(float* scale, float* recip, const float* k, const float* v,
+                                   int H, cudaStream_t stream);
+
+// Calibration: amax over the finite values of bf16 K and V rows [n][H][D],
+// per kv head or per tensor, turned into scale = amax / fmt_max (1 if amax is
+// 0) and its reciprocal in scale / recip ([2][H]).  amax_scratch: 2 * H words.
+cudaError_t launch_calibrate(const Geometry& g, const void* k, const void* v, int n, bool per_head,
+                             unsigned* amax_scratch, float* scale, float* recip,
+                             cudaStream_t stream);
 
 // Decode attention plan: how many warp workers and how much workspace.
 struct DecodePlan {
@@ -72,7 +93,7 @@ bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_pe
 cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePlan& plan,
                           const void* q, int num_q_heads, const int32_t* page_table,
                           int max_pages_per_seq, const int32_t* seq_lens, int batch,
-                          float sm_scale, float k_factor, float v_factor, void* out,
-                          void* workspace, int* err, cudaStream_t stream);
+                          float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
+                          void* out, void* workspace, int* err, cudaStream_t stream);
 
 }  // namespace kvq

@@ -37,6 +37,8 @@ struct StoreArgs {
   bool fast_div;         // scales in [2^-80, 2^80]: reciprocal-based division is exact
   int64_t num_pages;
   int* err;
+  const float* hs[2];    // per-kv-head scales of K, V (per-head kernels only)
+  const float* hr[2];    // their reciprocals
 };
 
 // Largest bf16 magnitude of the 16 values as fp32 bits; NaN propagates, so
@@ -171,8 +173,10 @@ __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t 
 // Grid-stride loop over items (token, block-of-16) of one of K / V (blockIdx.y),
 // software-pipelined: the next item's 32 input bytes and slot id are loaded
 // before the current block is encoded, so every thread keeps a load in flight
-// while it computes.
-template <kvq_format F>
+// while it computes.  PH: the scale of each item's kv head comes from the
+// per-head arrays ("Quantized KV cache" (vLLM), Supported schemes:
+// per-attention-head scales) instead of the per-tensor launch argument.
+template <kvq_format F, bool PH>
 __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
   const int kv = blockIdx.y;
   // the item index advances by a constant stride, split once into (tokens, blocks)
@@ -188,6 +192,8 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
   const uint16_t* const xin = kv ? a.x[1] : a.x[0];
   uint8_t* const dat = kv ? a.data[1] : a.data[0];
   uint8_t* const scl = kv ? a.scales[1] : a.scales[0];
+  const float* const hsp = kv ? a.hs[1] : a.hs[0];
+  const float* const hrp = kv ? a.hr[1] : a.hr[0];
   const int64_t tok_elems = (int64_t)a.H * a.D;  // input row of one token; block `pair` at pair * 16
   const int64_t capacity = a.num_pages * a.P;
 
@@ -224,7 +230,12 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
         off = slot - page * a.P;
       }
       const int64_t r = (page * a.H + h) * a.P + off;  // destination row
-      store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, s, rs, a.fast_div);
+      if constexpr (PH) {
+        const float sh = __ldg(hsp + h), rh = __ldg(hrp + h);
+        store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, sh, rh, sh >= 0x1p-80f && sh <= 0x1p80f);
+      } else {
+        store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, s, rs, a.fast_div);
+      }
     }
     if (!more) break;
     tok = ntok;
@@ -245,6 +256,7 @@ struct DequantArgs {
   int H, D, P;
   int64_t num_pages;
   int* err;
+  const float* hs[2];  // per-kv-head scales of K, V, or null (per tensor)
 };
 
 template <kvq_format F>
@@ -254,7 +266,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
   const uint8_t* const dat = kv ? a.data[1] : a.data[0];
   const uint8_t* const scl = kv ? a.scales[1] : a.scales[0];
   uint16_t* const outp = kv ? a.out[1] : a.out[0];
-  const float s_kv = kv ? a.s[1] : a.s[0];
+  const float s_tensor = kv ? a.s[1] : a.s[0];
+  const float* const hsp = kv ? a.hs[1] : a.hs[0];
   for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < a.items;
        it += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = it / nb;
@@ -272,6 +285,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
     }
     const int64_t page = slot / a.P, off = slot - page * a.P;
     const int64_t r = (page * a.H + h) * a.P + off;
+    const float s_kv = hsp ? __ldg(hsp + h) : s_tensor;
     if (F == KVQ_BF16) {
       const uint4* s4 = reinterpret_cast<const uint4*>(dat + r * (a.D * 2) + blk * 32);
       dst[0] = __ldg(s4);
@@ -334,17 +348,17 @@ int grid_for(int64_t items) {
 // more CTAs than there are items.  Measured on the 131072-token 70B-layer store:
 // one wave reaches 0.72 (bf16) to 0.89 (FP4 block-16) of the copy bandwidth,
 // four to eight waves 0.98 / 0.90, with the quantizing formats flat from four up.
-template <kvq_format F>
+template <kvq_format F, bool PH>
 cudaError_t launch_store_as(const StoreArgs& a, int64_t items, cudaStream_t stream) {
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, store_kernel<F>, 256, 0);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, store_kernel<F, PH>, 256, 0);
   if (e != cudaSuccess) return e;
   const int64_t wave = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) * 8 / 2);
   const int64_t need = (items + 255) / 256;
   dim3 grid((unsigned)std::min(wave, need), 2);
-  store_kernel<F><<<grid, 256, 0, stream>>>(a);
+  store_kernel<F, PH><<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -356,8 +370,8 @@ inline int log2_if_pow2(int v) {
 }
 
 cudaError_t launch_store(const Geometry& g, const LayerView& L, const void* k, const void* v,
-                         const int64_t* slots, int num_tokens, float s_k, float s_v, int* err,
-                         cudaStream_t stream) {
+                         const int64_t* slots, int num_tokens, float s_k, float s_v,
+                         const HeadScales& hs, int* err, cudaStream_t stream) {
   StoreArgs a;
   a.x[0] = static_cast<const uint16_t*>(k);
   a.x[1] = static_cast<const uint16_t*>(v);
@@ -384,19 +398,30 @@ cudaError_t launch_store(const Geometry& g, const LayerView& L, const void* k, c
   a.err = err;
   const int64_t items = (int64_t)num_tokens * a.hb;
   if (items == 0) return cudaSuccess;
+  a.hs[0] = hs.scale[0];
+  a.hs[1] = hs.scale[1];
+  a.hr[0] = hs.recip[0];
+  a.hr[1] = hs.recip[1];
+  const bool ph = hs.scale[0] != nullptr;
   switch (g.fmt) {
-    case KVQ_BF16: return launch_store_as<KVQ_BF16>(a, items, stream);
-    case KVQ_FP8_E4M3: return launch_store_as<KVQ_FP8_E4M3>(a, items, stream);
-    case KVQ_FP8_E5M2: return launch_store_as<KVQ_FP8_E5M2>(a, items, stream);
-    case KVQ_FP4_BLOCK16: return launch_store_as<KVQ_FP4_BLOCK16>(a, items, stream);
-    case KVQ_NVFP4: return launch_store_as<KVQ_NVFP4>(a, items, stream);
+    case KVQ_BF16: return launch_store_as<KVQ_BF16, false>(a, items, stream);
+    case KVQ_FP8_E4M3:
+      return ph ? launch_store_as<KVQ_FP8_E4M3, true>(a, items, stream)
+                : launch_store_as<KVQ_FP8_E4M3, false>(a, items, stream);
+    case KVQ_FP8_E5M2:
+      return ph ? launch_store_as<KVQ_FP8_E5M2, true>(a, items, stream)
+                : launch_store_as<KVQ_FP8_E5M2, false>(a, items, stream);
+    case KVQ_FP4_BLOCK16: return launch_store_as<KVQ_FP4_BLOCK16, false>(a, items, stream);
+    case KVQ_NVFP4:
+      return ph ? launch_store_as<KVQ_NVFP4, true>(a, items, stream)
+                : launch_store_as<KVQ_NVFP4, false>(a, items, stream);
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_dequantize(const Geometry& g, const LayerView& L, const int64_t* slots,
-                              int num_tokens, float s_k, float s_v, void* k_out, void* v_out,
-                              int* err, cudaStream_t stream) {
+                              int num_tokens, float s_k, float s_v, const HeadScales& hs,
+                              void* k_out, void* v_out, int* err, cudaStream_t stream) {
   DequantArgs a;
   a.data[0] = L.k_data;
   a.data[1] = L.v_data;
@@ -413,6 +438,8 @@ cudaError_t launch_dequantize(const Geometry& g, const LayerView& L, const int64
   a.P = g.page_size;
   a.num_pages = g.num_pages;
   a.err = err;
+  a.hs[0] = hs.scale[0];
+  a.hs[1] = hs.scale[1];
   if (a.items == 0) return cudaSuccess;
   dim3 grid(grid_for(a.items), 2);
   switch (g.fmt) {
@@ -422,6 +449,151 @@ cudaError_t launch_dequantize(const Geometry& g, const LayerView& L, const int64
     case KVQ_FP4_BLOCK16: dequant_kernel<KVQ_FP4_BLOCK16><<<grid, 256, 0, stream>>>(a); break;
     case KVQ_NVFP4: dequant_kernel<KVQ_NVFP4><<<grid, 256, 0, stream>>>(a); break;
   }
+  return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------------------------
+// Per-head scales and calibration ("Quantized KV cache" (vLLM features page):
+// Supported schemes -- one scale per kv head; Scale calibration approaches --
+// scales estimated on the fly from a batch of tokens, then fixed).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kSetChunk = 64;  // heads per set-scales launch (values travel as arguments)
+
+struct SetScalesArgs {
+  float v[2][kSetChunk];  // K, V scales of heads h0 .. h0 + count - 1
+  int H, h0, count;
+  float* scale;
+  float* recip;
+};
+
+__global__ void __launch_bounds__(2 * kSetChunk) set_scales_kernel(SetScalesArgs a) {
+  const int kv = threadIdx.x / kSetChunk, j = threadIdx.x % kSetChunk;
+  if (j < a.count) {
+    const float s = a.v[kv][j];
+    a.scale[kv * a.H + a.h0 + j] = s;
+    a.recip[kv * a.H + a.h0 + j] = 1.0f / s;  // IEEE division
+  }
+}
+
+constexpr int kCalSmemHeads = 1024;  // heads reduced in shared memory (more go to global atomics)
+
+struct CalArgs {
+  const uint16_t* x[2];  // K, V bf16 [n][H][D]
+  int64_t n;
+  int H, nb, hb;         // kv heads, 16-element blocks per row, H * nb
+  unsigned* amax;        // [2][H] bf16 magnitude bits of the largest finite |x|
+};
+
+// Largest finite bf16 magnitude among 16 values, as its 16-bit pattern
+// (non-finite values have magnitude patterns >= 0x7F80 and are dropped).
+__device__ __forceinline__ uint32_t block_amax_finite(const uint4 lo, const uint4 hi) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint32_t m = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t x = w[i] & 0x7FFF7FFFu;
+    x &= ~__vcmpgeu2(x, 0x7F807F80u);
+    m = __vmaxu2(m, x);
+  }
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+__global__ void __launch_bounds__(256) calib_amax_kernel(CalArgs a) {
+  __shared__ unsigned smax[kCalSmemHeads];
+  const int kv = blockIdx.y;
+  const int hsm = min(a.H, kCalSmemHeads);
+  for (int i = threadIdx.x; i < hsm; i += blockDim.x) smax[i] = 0u;
+  __syncthreads();
+  const uint16_t* const x = kv ? a.x[1] : a.x[0];
+  unsigned* const gmax = a.amax + (size_t)kv * a.H;
+  const long long items = a.n * a.hb;
+  const long long row = (long long)a.hb * 16;  // elements per token
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+       it += (long long)gridDim.x * blockDim.x) {
+    const long long tok = it / a.hb;
+    const int pair = (int)(it - tok * a.hb);
+    const int h = pair / a.nb;
+    const uint4* src = reinterpret_cast<const uint4*>(x + tok * row + (long long)pair * 16);
+    const uint32_t m = block_amax_finite(__ldg(src), __ldg(src + 1));
+    if (m != 0u) {
+      if (h < kCalSmemHeads) atomicMax(&smax[h], m);
+      else atomicMax(gmax + h, m);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < hsm; i += blockDim.x)
+    if (smax[i] != 0u) atomicMax(gmax + i, smax[i]);
+}
+
+// scale = amax / fmt_max (IEEE fp32 division), 1 when amax is 0; per tensor:
+// the largest amax over the heads serves every head.
+__global__ void __launch_bounds__(256) calib_finalize_kernel(const unsigned* amax, int H,
+                                                             bool per_head, float fmt_max,
+                                                             float* scale, float* recip) {
+  __shared__ unsigned tmax[2];
+  if (threadIdx.x < 2) tmax[threadIdx.x] = 0u;
+  __syncthreads();
+  if (!per_head)
+    for (int i = threadIdx.x; i < 2 * H; i += blockDim.x) atomicMax(&tmax[i / H], amax[i]);
+  __syncthreads();
+  for (int i = threadIdx.x; i < 2 * H; i += blockDim.x) {
+    const unsigned bits = per_head ? amax[i] : tmax[i / H];
+    const float am = __uint_as_float(bits << 16);
+    const float sc = am > 0.f ? am / fmt_max : 1.0f;
+    scale[i] = sc;
+    recip[i] = 1.0f / sc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_set_head_scales(float* scale, float* recip, const float* k, const float* v,
+                                   int H, cudaStream_t stream) {
+  for (int h0 = 0; h0 < H; h0 += kSetChunk) {
+    SetScalesArgs a;
+    a.H = H;
+    a.h0 = h0;
+    a.count = std::min(kSetChunk, H - h0);
+    for (int j = 0; j < kSetChunk; ++j) {
+      a.v[0][j] = j < a.count ? k[h0 + j] : 1.0f;
+      a.v[1][j] = j < a.count ? v[h0 + j] : 1.0f;
+    }
+    a.scale = scale;
+    a.recip = recip;
+    set_scales_kernel<<<1, 2 * kSetChunk, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_calibrate(const Geometry& g, const void* k, const void* v, int n, bool per_head,
+                             unsigned* amax_scratch, float* scale, float* recip,
+                             cudaStream_t stream) {
+  const float fmt_max = g.fmt == KVQ_FP8_E4M3 ? 448.0f
+                        : g.fmt == KVQ_FP8_E5M2 ? 57344.0f
+                                                : 6.0f * 448.0f;  // NVFP4: E2M1 max x E4M3 max
+  cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned) * 2 * (size_t)g.kv_heads, stream);
+  if (e != cudaSuccess) return e;
+  CalArgs a;
+  a.x[0] = static_cast<const uint16_t*>(k);
+  a.x[1] = static_cast<const uint16_t*>(v);
+  a.n = n;
+  a.H = g.kv_heads;
+  a.nb = g.head_dim / 16;
+  a.hb = a.H * a.nb;
+  a.amax = amax_scratch;
+  const int64_t items = (int64_t)n * a.hb;
+  if (items > 0) {
+    dim3 grid(grid_for(items), 2);
+    calib_amax_kernel<<<grid, 256, 0, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  calib_finalize_kernel<<<1, 256, 0, stream>>>(amax_scratch, g.kv_heads, per_head, fmt_max, scale,
+                                               recip);
   return cudaGetLastError();
 }
 
