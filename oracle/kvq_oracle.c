@@ -15,7 +15,7 @@
  *           INT8, FP8, INT4: measured numbers; When to enable.
  *   [NVFP4] "SGLang PR #21954 analysis: NVFP4 KV cache" (secrett2633 blog):
  *           Code analysis 1 (fp4_kv_cache_quant_method.py), Review feedback.
- *   [VLLM-KV] "Quantized KV cache" (vLLM features page on the data-sketchers
+ *   [VLLM]  "Quantized KV cache" (vLLM features page on the data-sketchers
  *           wiki): Supported schemes; Scale calibration approaches.
  *   The formats themselves are the OCP 8-bit floating point (OFP8) and OCP
  *   Microscaling (MX) v1.0 definitions that [QKV] names.
@@ -42,10 +42,10 @@
  *   R8  Dequantize: out = bf16_RNE(fp32(dec(code) * S)).
  *   R9  Attention: q head j reads kv head floor(j / G), G = Hq / Hkv; a
  *       sequence of length 0 gives an all-zero output.
- *   R15 Per-attention-head scales ([VLLM-KV] Supported schemes): the FP8
+ *   R15 Per-attention-head scales ([VLLM] Supported schemes): the FP8
  *       scale (and the NVFP4 global scale) of kv head h is scales[h] of K or
  *       V; per-tensor scales are the case where every head has the same one.
- *   R16 Calibration from a batch of K or V rows ([VLLM-KV] Scale calibration
+ *   R16 Calibration from a batch of K or V rows ([VLLM] Scale calibration
  *       approaches, random-token mode; [QKV] Scaling factors): amax over the
  *       finite values (per tensor, or per kv head); scale = amax / M in fp32
  *       with M = 448 (E4M3), 57344 (E5M2), 6 * 448 = 2688 (NVFP4 global scale,
