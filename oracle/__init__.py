@@ -214,5 +214,14 @@ class OracleCache:
                                           float(sm_scale), _ptr(out))
         return out, rc
 
+    def extend_attention(self, q_bf16: np.ndarray, q_seq: np.ndarray, q_len: np.ndarray,
+                         page_table: np.ndarray, sm_scale: float):
+        """Extend (chunked-prefill) attention: query token i of sequence q_seq[i]
+        attends to that sequence's tokens [0, q_len[i]) (its causal prefix,
+        itself included).  This is decode attention with one row per query
+        token: page-table row page_table[q_seq[i]] and length q_len[i]."""
+        rows = np.asarray(page_table, np.int32)[np.asarray(q_seq, np.int64)]
+        return self.decode_attention(q_bf16, rows, np.asarray(q_len, np.int32), sm_scale)
+
     def row_index(self, slot: int, h: int) -> int:
         return ((slot // self.P) * self.H + h) * self.P + slot % self.P

@@ -132,3 +132,30 @@ def test_b_list_selects_sequences(orc):
     full, _ = c.decode_attention(wl.q(), wl.page_table, wl.seq_lens, wl.sm_scale)
     part, _ = c.decode_attention(wl.q(), wl.page_table, wl.seq_lens, wl.sm_scale, b_list=[2])
     assert np.array_equal(part[2], full[2]) and (part[:2] == 0).all()
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "nvfp4"])
+def test_extend_attention_matches_torch_causal_sdpa(orc, fmt):
+    """A chunk of new query tokens at the end of each sequence: query i sees the
+    sequence's tokens up to and including its own position (causal prefill)."""
+    wl = synth.make_workload(f"x_{fmt}", fmt, Hq=8, Hkv=2, D=64, seq_lens=[45, 20], seed=13)
+    c = _store_all(orc, wl)
+    chunk = [5, 3]                                 # newest tokens of each sequence are queries
+    q_seq = np.concatenate([np.full(n, b) for b, n in enumerate(chunk)])
+    q_len = np.concatenate([np.arange(wl.seq_lens[b] - n, wl.seq_lens[b]) + 1 for b, n in enumerate(chunk)])
+    q = synth.to_bf16_bits(torch.randn(len(q_seq), wl.Hq, wl.D, generator=torch.Generator().manual_seed(4)))
+    out, rc = c.extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
+    assert rc == 0
+    qd = torch.from_numpy(q.view(np.int16).copy()).view(torch.bfloat16).double()
+    i0 = 0
+    for b, n in enumerate(chunk):
+        T = int(wl.seq_lens[b])
+        K = _exact_kv(fmt, c, wl, b, "k").permute(1, 0, 2)[None]      # [1, Hkv, T, D]
+        V = _exact_kv(fmt, c, wl, b, "v").permute(1, 0, 2)[None]
+        Q = qd[i0:i0 + n].permute(1, 0, 2)[None]                       # [1, Hq, n, D]
+        # query j sits at position T - n + j: bottom-right aligned causal mask
+        mask = torch.ones(n, T, dtype=torch.bool).tril(diagonal=T - n)
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask,
+                                                               scale=wl.sm_scale, enable_gqa=True)
+        np.testing.assert_allclose(out[i0:i0 + n], ref[0].permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
+        i0 += n
