@@ -191,6 +191,33 @@ kvq_status kvq_decode_attention(kvq_cache* cache, int layer, const void* q_bf16,
                                 void* out_bf16, void* workspace, size_t workspace_bytes,
                                 kvq_stream stream);
 
+/*
+ * Extend (chunked-prefill) attention over the cache of `layer` ([NVFP4] Code
+ * analysis 1: the prefill / extend path reads the previously stored,
+ * quantized KV; here it is read in place instead of through a dequantized
+ * workspace).  Query token i belongs to sequence q_seq[i] and attends to that
+ * sequence's tokens [0, q_len[i]) -- its causal prefix, itself included, so
+ * the new tokens must be stored first:
+ *   out[i][j] = sum_t softmax_t(sm_scale * q[i][j] . K^[t]) V^[t],
+ *   t < q_len[i], token t in page page_table[q_seq[i]][t / page_size].
+ *   q_bf16, out_bf16: [num_q_tokens][num_q_heads][head_dim] bf16.
+ *   q_seq, q_len:     int32 [num_q_tokens] device arrays; 0 <= q_seq[i] <
+ *                     num_seqs, 0 <= q_len[i] <= max_pages_per_seq * page_size.
+ *   page_table:       int32 [num_seqs][max_pages_per_seq].
+ *   workspace:        kvq_decode_workspace_size(cache, num_q_tokens,
+ *                     num_q_heads, max_pages_per_seq) bytes.
+ * Each query token is one decode query over its prefix (the same kernels; a
+ * chunk's queries re-read the shared prefix, mostly from L2).  Out-of-range
+ * q_seq, q_len or page ids raise KVQ_ERR_DEVICE_RANGE in the device error word
+ * and zero that query's output.  Other rules and errors as for
+ * kvq_decode_attention.
+ */
+kvq_status kvq_extend_attention(kvq_cache* cache, int layer, const void* q_bf16, int num_q_heads,
+                                int num_q_tokens, const int32_t* q_seq, const int32_t* q_len,
+                                const int32_t* page_table, int num_seqs, int max_pages_per_seq,
+                                float sm_scale, void* out_bf16, void* workspace,
+                                size_t workspace_bytes, kvq_stream stream);
+
 /* Bytes of workspace kvq_decode_attention needs for these sizes (0 on invalid
  * arguments; see kvq_last_error_string). */
 size_t kvq_decode_workspace_size(const kvq_cache* cache, int batch, int num_q_heads,

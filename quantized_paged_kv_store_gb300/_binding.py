@@ -35,6 +35,8 @@ def _load():
         "kvq_layer_head_scales": ([vp, i32, ctypes.POINTER(f32), ctypes.POINTER(f32), vp], i32),
         "kvq_decode_attention": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp, sz, vp], i32),
         "kvq_decode_workspace_size": ([vp, i32, i32, i32], sz),
+        "kvq_extend_attention": ([vp, i32, vp, i32, i32, vp, vp, vp, i32, i32, f32, vp, vp, sz, vp],
+                                 i32),
         "kvq_decode_attention_noalloc": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp], i32),
         "kvq_dequantize": ([vp, i32, vp, i32, vp, vp, vp], i32),
         "kvq_cache_layout": ([vp, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
@@ -166,6 +168,17 @@ def kvq_decode_attention(handle, layer, q, page_table, seq_lens, sm_scale, out, 
            "kvq_decode_attention")
 
 
+def kvq_extend_attention(handle, layer, q, q_seq, q_len, page_table, sm_scale, out, workspace,
+                         stream=None):
+    """q, out: bf16 [n][Hq][D]; q_seq, q_len: int32 [n]; page_table int32 [S][max_pages]."""
+    n, Hq, _ = q.shape
+    _check(lib.kvq_extend_attention(ctypes.c_void_p(handle), layer, _ptr(q), Hq, n, _ptr(q_seq),
+                                    _ptr(q_len), _ptr(page_table), int(page_table.shape[0]),
+                                    int(page_table.shape[1]), float(sm_scale), _ptr(out),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)), "kvq_extend_attention")
+
+
 def kvq_decode_attention_noalloc(handle, layer, q, page_table, seq_lens, sm_scale, out,
                                  stream=None):
     """kvq_decode_attention with the library's static scratch instead of a
@@ -250,6 +263,18 @@ class KVQCache:
             workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
         kvq_decode_attention(self.handle, layer, q, page_table, seq_lens, sm_scale, out, workspace,
                              stream)
+        return out
+
+    def extend_attention(self, layer, q, q_seq, q_len, page_table, sm_scale, out=None,
+                         workspace=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        if workspace is None:
+            n = self.workspace_size(q.shape[0], q.shape[1], page_table.shape[1])
+            workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+        kvq_extend_attention(self.handle, layer, q, q_seq, q_len, page_table, sm_scale, out,
+                             workspace, stream)
         return out
 
     def dequantize(self, layer, slot_mapping, stream=None):

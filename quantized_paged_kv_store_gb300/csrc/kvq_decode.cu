@@ -493,7 +493,7 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
 
   // ---- page ids, prefetched one window (32 tiles) ahead ----------------------
   const int tiles_per_page = a.P / kTile;
-  const int32_t* prow = a.page_table + (long long)b * a.max_pages;
+  const int32_t* prow = a.page_table + (long long)pt_row_of(a, b) * a.max_pages;
   auto load_pid = [&](int win) -> int {
     const int t = t0 + win * kPidWin + lane;
     return (t < t1) ? __ldg(prow + t / tiles_per_page) : -1;
@@ -738,7 +738,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs
     int nt = 0;
     if (b < a.B) {
       const int T = __ldg(a.seq_lens + b);
-      if (T < 0 || T > a.max_pages * a.P) bad_len = true;
+      if (T < 0 || T > a.max_pages * a.P || pt_row_of(a, b) < 0) bad_len = true;
       nt = tiles_of(a, b);
     }
     if (w == 0) {  // publish the per-sequence tile prefix for the merge
@@ -897,7 +897,8 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
                           const void* q, int num_q_heads, const int32_t* page_table,
                           int max_pages_per_seq, const int32_t* seq_lens, int batch,
                           float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
-                          void* out, void* workspace, int* err, cudaStream_t stream) {
+                          const int32_t* pt_rows, int pt_nrows, void* out, void* workspace,
+                          int* err, cudaStream_t stream) {
   DecodeArgs a;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.part_o = reinterpret_cast<float*>(ws);
@@ -929,6 +930,8 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
   a.vfac = hs.scale[1];
   a.qscale = sm_scale * 1.4426950408889634f * (a.kfac ? 1.0f : k_factor);
   a.v_factor = v_factor;
+  a.pt_rows = pt_rows;
+  a.pt_nrows = pt_nrows;
   a.err = err;
   if (batch == 0) return cudaSuccess;
   cudaError_t e = cudaErrorInvalidValue;

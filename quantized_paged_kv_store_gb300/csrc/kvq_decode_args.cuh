@@ -31,6 +31,8 @@ struct DecodeArgs {
   int* err;
   const float* kfac;  // per-kv-head K scales (or null: per tensor)
   const float* vfac;  // per-kv-head V scales (or null)
+  const int32_t* pt_rows;  // extend: page-table row of each query token b (or null: row b)
+  int pt_nrows;            // rows of the page table when pt_rows is set
 };
 
 
@@ -42,9 +44,18 @@ __device__ __forceinline__ float ex2(float x) {
   return r;
 }
 
-// Tiles of sequence b (0 for an empty or invalid length).
+// Page-table row of query b: b itself for decode; for extend attention the
+// row its q_seq entry names, or -1 if that is out of range.
+__device__ __forceinline__ int pt_row_of(const DecodeArgs& a, int b) {
+  if (!a.pt_rows) return b;
+  const int r = __ldg(a.pt_rows + b);
+  return (r >= 0 && r < a.pt_nrows) ? r : -1;
+}
+
+// Tiles of sequence (query) b (0 for an empty or invalid length or row).
 __device__ __forceinline__ int tiles_of(const DecodeArgs& a, int b) {
   const int T = __ldg(a.seq_lens + b);
+  if (pt_row_of(a, b) < 0) return 0;
   return (T > 0 && T <= a.max_pages * a.P) ? (T + kTile - 1) / kTile : 0;
 }
 

@@ -94,6 +94,7 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
                           const void* q, int num_q_heads, const int32_t* page_table,
                           int max_pages_per_seq, const int32_t* seq_lens, int batch,
                           float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
-                          void* out, void* workspace, int* err, cudaStream_t stream);
+                          const int32_t* pt_rows, int pt_nrows, void* out, void* workspace,
+                          int* err, cudaStream_t stream);
 
 }  // namespace kvq

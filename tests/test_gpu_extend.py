@@ -1,0 +1,95 @@
+"""GPU parity of extend (chunked-prefill) attention over the quantized cache:
+query token i of sequence q_seq[i] attends to that sequence's tokens
+[0, q_len[i]).  Compared with the oracle's fp64 attention within the decode
+tolerance (excess over bf16 rounding)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import (assert_attention_close, bits_to_cuda, cuda_to_bits, gpu_cache_for,
+                      oracle_cache_for, store_layer)
+
+pytestmark = pytest.mark.gpu
+FORMATS = ["bf16", "fp8_e4m3", "fp8_e5m2", "fp4_mx_block16", "nvfp4"]
+
+
+def _queries(wl, chunk, seed):
+    """The newest chunk[b] tokens of each sequence b as queries (causal prefill
+    of the chunk), plus their bf16 query rows."""
+    q_seq = np.concatenate([np.full(n, b, np.int32) for b, n in enumerate(chunk)])
+    q_len = np.concatenate([np.arange(int(wl.seq_lens[b]) - n, int(wl.seq_lens[b])) + 1
+                            for b, n in enumerate(chunk)]).astype(np.int32)
+    g = torch.Generator().manual_seed(seed)
+    q = synth.to_bf16_bits(torch.randn(len(q_seq), wl.Hq, wl.D, generator=g))
+    return q, q_seq, q_len
+
+
+def _gpu_extend(c, wl, q, q_seq, q_len):
+    out = c.extend_attention(0, bits_to_cuda(q), torch.from_numpy(q_seq).cuda(),
+                             torch.from_numpy(q_len).cuda(), torch.from_numpy(wl.page_table).cuda(),
+                             wl.sm_scale)
+    torch.cuda.synchronize()
+    return synth.bf16_bits_to_float(cuda_to_bits(out)).astype(np.float64)
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_extend_matches_oracle(kvq, orc, cuda, fmt):
+    wl = synth.make_workload(f"ext_{fmt}", fmt, Hq=16, Hkv=4, seq_lens=[300, 65, 130, 17], seed=31)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    q, q_seq, q_len = _queries(wl, [24, 1, 16, 17], seed=2)
+    got = _gpu_extend(c, wl, q, q_seq, q_len)
+    assert c.device_error() == 0
+    ref, rc = oracle_cache_for(orc, wl).extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
+    assert rc == 0
+    assert_attention_close(got, ref, f"{fmt} extend")
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "nvfp4"])
+def test_extend_70b_shape_random_positions(kvq, orc, cuda, fmt):
+    """70B head layout (64 q heads, 8 kv heads); queries at arbitrary positions
+    of two long sequences, interleaved."""
+    wl = synth.make_workload(f"ext70_{fmt}", fmt, Hq=64, Hkv=8, seq_lens=[2000, 777], seed=7)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    rng = np.random.default_rng(5)
+    q_seq = rng.integers(0, 2, 40).astype(np.int32)
+    q_len = np.array([rng.integers(1, int(wl.seq_lens[b]) + 1) for b in q_seq], np.int32)
+    q = synth.to_bf16_bits(torch.randn(40, wl.Hq, wl.D, generator=torch.Generator().manual_seed(1)))
+    got = _gpu_extend(c, wl, q, q_seq, q_len)
+    assert c.device_error() == 0
+    ref, rc = oracle_cache_for(orc, wl).extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
+    assert rc == 0
+    assert_attention_close(got, ref, f"{fmt} extend 70B")
+
+
+def test_extend_last_token_is_decode(kvq, cuda):
+    """One query per sequence at its last position is exactly a decode call."""
+    wl = synth.make_workload("ext_dec", "nvfp4", Hq=16, Hkv=2, seq_lens=[500, 77, 0, 33], seed=4)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    q = bits_to_cuda(wl.q())
+    pt = torch.from_numpy(wl.page_table).cuda()
+    dec = c.decode_attention(0, q, pt, torch.from_numpy(wl.seq_lens).cuda(), wl.sm_scale)
+    ext = c.extend_attention(0, q, torch.arange(wl.B, dtype=torch.int32, device="cuda"),
+                             torch.from_numpy(wl.seq_lens).cuda(), pt, wl.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(dec.view(torch.int16), ext.view(torch.int16))
+
+
+def test_extend_bad_rows_and_lengths(kvq, cuda):
+    wl = synth.make_workload("ext_bad", "fp8_e4m3", Hq=8, Hkv=2, seq_lens=[40, 40], seed=2)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    q, _, _ = _queries(wl, [2, 2], seed=3)
+    q_seq = np.array([0, 5, 1, -1], np.int32)          # rows 5 and -1 do not exist
+    q_len = np.array([40, 10, 40, 10], np.int32)
+    got = _gpu_extend(c, wl, q, q_seq, q_len)
+    assert c.device_error() == kvq._binding._STATUS_CODES["KVQ_ERR_DEVICE_RANGE"]
+    assert (got[1] == 0).all() and (got[3] == 0).all()
+    assert (got[0] != 0).any() and (got[2] != 0).any()
+    q_len = np.array([40, wl.max_pages * wl.P + 1, 40, 3], np.int32)
+    got = _gpu_extend(c, wl, q, np.array([0, 1, 1, 0], np.int32), q_len)
+    assert c.device_error() == kvq._binding._STATUS_CODES["KVQ_ERR_DEVICE_RANGE"]
+    assert (got[1] == 0).all() and (got[3] != 0).any()
