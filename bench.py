@@ -64,6 +64,8 @@ def parse_args(argv=None):
     p.add_argument("--store-formats", default=None, help="comma-separated subset for --store")
     p.add_argument("--store-only", action="store_true",
                    help="run only the --store measurement (no decode line)")
+    p.add_argument("--next", default=None, help="time the per-head-scale decode, on-device "
+                   "calibration and extend attention paths, one JSON line each appended to this file")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=32,
@@ -486,6 +488,136 @@ def run_sweep(args):
                                             "clocks": r["clocks"]}) + "\n")
 
 
+def _time_calls(fn, steps, warmup):
+    """Mean CUDA-event milliseconds of fn() over `steps` calls after `warmup`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
+        fn()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    return statistics.fmean(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+
+
+def run_next(args):
+    """Per-head scales (calibrated on the device), calibration itself, and extend
+    attention, on the benchmark's shapes; one JSON line per measurement."""
+    import numpy as np
+    import torch
+    import quantized_paged_kv_store_gb300 as kvq
+    import synth
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak, _ = peak_hbm()
+    steps = max(20, min(args.steps, 300))
+    warm = max(3, min(args.warmup, 10))
+    out = []
+
+    def emit(d):
+        if rank == 0:
+            with open(args.next, "a") as f:
+                f.write(json.dumps(d) + "\n")
+        out.append(d)
+
+    # 1) decode over a layer whose scales are per kv head (calibrated on the device
+    #    from sequence 0's rows) against the same layer with per-tensor scales
+    for fmt in ("nvfp4", "fp8_e4m3"):
+        wl = make_workload(fmt, args.seed + 7919 * rank, None, args.batch)
+        ks, vs = wl.kv_all(0)
+        d_q = synth_to_cuda(wl.q(0))
+        d_pt = torch.from_numpy(wl.page_table).to(dev)
+        d_sl = torch.from_numpy(wl.seq_lens).to(dev)
+        d_out = torch.empty_like(d_q)
+        dbytes = algorithmic_bytes(wl, fmt)
+        for mode in ("per_tensor", "per_head_calibrated"):
+            cache = kvq.KVQCache(fmt, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
+            if mode == "per_head_calibrated":
+                cache.calibrate_scales(0, synth_to_cuda(ks[0]), synth_to_cuda(vs[0]), per_head=True)
+                scales = None
+            else:
+                scales = [float(x) for x in wl.scales(0)]
+            for b in range(wl.B):
+                cache.quantize_and_store(0, synth_to_cuda(ks[b]), synth_to_cuda(vs[b]),
+                                         torch.from_numpy(wl.slots(b)).to(dev), scales)
+            ws = torch.empty(cache.workspace_size(wl.B, wl.Hq, wl.max_pages), dtype=torch.uint8,
+                             device=dev)
+            ms = _time_calls(lambda: cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale, d_out, ws),
+                             steps, warm)
+            if cache.device_error() != 0:
+                raise RuntimeError("device error in the per-head decode measurement")
+            gbs = dbytes / (ms * 1e-3) / 1e9
+            emit({"path": "decode", "scales": mode, "format": fmt, "workload": wl.name,
+                  "batch": wl.B, "tokens_cached": int(wl.seq_lens.sum()), "ms_per_call": round(ms, 5),
+                  "GBps": round(gbs, 1), "frac": round(gbs / peak, 4)})
+            cache.close()
+
+    # 2) on-device calibration of the 70B-layer 8 x 16K prefill (per kv head):
+    #    an amax reduction over K and V; one cache layer per call (a layer's
+    #    scales are fixed once)
+    wl = synth.cfg3_fp4b16_70b(seed=args.seed + 7919 * rank)
+    ks, vs = wl.kv_all(0)
+    k = synth_to_cuda(np.concatenate(ks))
+    v = synth_to_cuda(np.concatenate(vs))
+    n = int(k.shape[0])
+    for fmt in ("fp8_e4m3", "nvfp4"):
+        cal = kvq.KVQCache(fmt, steps + warm, wl.Hkv, wl.D, 16, 1)
+        layer = [0]
+
+        def calibrate():
+            cal.calibrate_scales(layer[0], k, v, per_head=True)
+            layer[0] += 1
+
+        ms = _time_calls(calibrate, steps, warm)
+        if cal.device_error() != 0:
+            raise RuntimeError("device error in the calibration measurement")
+        nbytes = 2 * n * wl.Hkv * wl.D * 2
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        emit({"path": "calibrate", "format": fmt, "tokens": n, "kv_heads": wl.Hkv,
+              "head_dim": wl.D, "per_head": True, "us_per_call": round(ms * 1e3, 2),
+              "bytes_per_call": nbytes, "GBps": round(gbs, 1), "frac": round(gbs / peak, 4)})
+        cal.close()
+
+    # 3) extend attention: a 16-token chunk at the end of every sequence of the
+    #    32K x 32 NVFP4 workload (512 queries); algorithmic bytes count every
+    #    sequence's cached prefix once, so re-reads across a chunk's queries show
+    #    as lost efficiency
+    fmt, chunk = "nvfp4", 16
+    wl = make_workload(fmt, args.seed + 7919 * rank, None, args.batch)
+    ks, vs = wl.kv_all(0)
+    cache = kvq.KVQCache(fmt, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
+    scales = [float(x) for x in wl.scales(0)]
+    for b in range(wl.B):
+        cache.quantize_and_store(0, synth_to_cuda(ks[b]), synth_to_cuda(vs[b]),
+                                 torch.from_numpy(wl.slots(b)).to(dev), scales)
+    q_seq = np.repeat(np.arange(wl.B, dtype=np.int32), chunk)
+    q_len = np.concatenate([np.arange(int(T) - chunk, int(T)) + 1 for T in wl.seq_lens]).astype(np.int32)
+    g = torch.Generator().manual_seed(args.seed)
+    d_q = synth_to_cuda(synth.to_bf16_bits(torch.randn(len(q_seq), wl.Hq, wl.D, generator=g)))
+    d_qs, d_ql = torch.from_numpy(q_seq).to(dev), torch.from_numpy(q_len).to(dev)
+    d_pt = torch.from_numpy(wl.page_table).to(dev)
+    d_out = torch.empty_like(d_q)
+    ws = torch.empty(cache.workspace_size(len(q_seq), wl.Hq, wl.max_pages), dtype=torch.uint8, device=dev)
+    ms = _time_calls(lambda: cache.extend_attention(0, d_q, d_qs, d_ql, d_pt, wl.sm_scale, d_out, ws),
+                     max(10, steps // 10), warm)
+    if cache.device_error() != 0:
+        raise RuntimeError("device error in the extend measurement")
+    prefix = int(wl.seq_lens.sum()) * wl.Hkv * KV_BYTES[fmt]
+    qo = 2 * len(q_seq) * wl.Hq * wl.D * 2
+    gbs = (prefix + qo) / (ms * 1e-3) / 1e9
+    emit({"path": "extend", "format": fmt, "workload": wl.name, "batch": wl.B, "chunk": chunk,
+          "queries": len(q_seq), "ms_per_call": round(ms, 4),
+          "queries_per_s": round(len(q_seq) / (ms * 1e-3), 1),
+          "GBps_prefix_once": round(gbs, 1), "frac": round(gbs / peak, 4),
+          "note": "each query re-reads its prefix (decode kernels); bytes counted once per sequence"})
+    cache.close()
+    return out
+
+
 # ------------------------------------------------------------ reference arm
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is a bounded sample of the
@@ -547,6 +679,9 @@ def main(argv=None):
     args = parse_args(argv)
     if args.store_only:
         run_store(args)
+        return
+    if args.next:
+        run_next(args)
         return
     if args.impl == "reference":
         run_reference(args)
