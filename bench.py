@@ -613,7 +613,7 @@ def run_next(args):
           "queries": len(q_seq), "ms_per_call": round(ms, 4),
           "queries_per_s": round(len(q_seq) / (ms * 1e-3), 1),
           "GBps_prefix_once": round(gbs, 1), "frac": round(gbs / peak, 4),
-          "note": "each query re-reads its prefix (decode kernels); bytes counted once per sequence"})
+          "note": "each K/V tile dequantized once per 64 (query, q head) rows; bytes counted once per sequence"})
     cache.close()
     return out
 

@@ -204,10 +204,11 @@ kvq_status kvq_decode_attention(kvq_cache* cache, int layer, const void* q_bf16,
  *   q_seq, q_len:     int32 [num_q_tokens] device arrays; 0 <= q_seq[i] <
  *                     num_seqs, 0 <= q_len[i] <= max_pages_per_seq * page_size.
  *   page_table:       int32 [num_seqs][max_pages_per_seq].
- *   workspace:        kvq_decode_workspace_size(cache, num_q_tokens,
- *                     num_q_heads, max_pages_per_seq) bytes.
- * Each query token is one decode query over its prefix (the same kernels; a
- * chunk's queries re-read the shared prefix, mostly from L2).  Out-of-range
+ *   workspace, workspace_bytes: not used (kept for the signature; may be
+ *                     NULL / 0).
+ * Every K/V tile of a sequence is read and dequantized once per 64 (query,
+ * q head) rows of a kv head, shared by those rows' queries (a chunk of 8
+ * queries at 8 q heads per kv head).  Out-of-range
  * q_seq, q_len or page ids raise KVQ_ERR_DEVICE_RANGE in the device error word
  * and zero that query's output.  Other rules and errors as for
  * kvq_decode_attention.

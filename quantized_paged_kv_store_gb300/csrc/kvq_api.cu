@@ -14,6 +14,7 @@
 #include <new>
 #include <vector>
 
+#include "kvq_decode_args.cuh"
 #include "kvq_internal.h"
 
 struct kvq_cache {
@@ -525,11 +526,33 @@ kvq_status kvq_extend_attention(kvq_cache* c, int layer, const void* q_bf16, int
                                 const int32_t* page_table, int num_seqs, int max_pages_per_seq,
                                 float sm_scale, void* out_bf16, void* workspace,
                                 size_t workspace_bytes, kvq_stream stream) {
-  if (num_q_tokens > 0 && (!q_seq || !q_len)) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
-  if (num_seqs <= 0) return fail(KVQ_ERR_INVALID_ARG, "num_seqs must be positive");
-  return attention_common(c, layer, q_bf16, num_q_heads, page_table, max_pages_per_seq, q_len,
-                          num_q_tokens, q_seq, num_seqs, sm_scale, out_bf16, workspace,
-                          workspace_bytes, stream);
+  (void)workspace;
+  (void)workspace_bytes;
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  const kvq::Geometry& g = c->geo;
+  if (num_q_tokens < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0 || num_seqs <= 0)
+    return fail(KVQ_ERR_INVALID_ARG, "invalid num_q_tokens / num_q_heads / max_pages / num_seqs");
+  if (!std::isfinite(sm_scale)) return fail(KVQ_ERR_INVALID_ARG, "sm_scale must be finite");
+  if (g.head_dim != kvq::kHeadDim)
+    return fail(KVQ_ERR_UNSUPPORTED, "extend attention supports head_dim == 128 only");
+  if (g.page_size % kvq::kTile != 0)
+    return fail(KVQ_ERR_UNSUPPORTED, "extend attention needs page_size %% 16 == 0");
+  if (num_q_heads % g.kv_heads != 0)
+    return fail(KVQ_ERR_UNSUPPORTED, "num_q_heads must be a multiple of kv_heads");
+  if (num_q_tokens == 0) return KVQ_OK;
+  if (!q_bf16 || !q_seq || !q_len || !page_table || !out_bf16)
+    return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+  if (!aligned16(q_bf16) || !aligned16(out_bf16))
+    return fail(KVQ_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if ((st = check_device(c))) return st;
+  float kf, vf;
+  tensor_scales(c, layer, &kf, &vf);
+  cudaError_t e = kvq::launch_extend(g, view(c, layer), q_bf16, num_q_heads, num_q_tokens, q_seq,
+                                     q_len, page_table, num_seqs, max_pages_per_seq, sm_scale, kf, vf,
+                                     head_scales(c, layer), out_bf16, c->err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "extend attention launch");
+  return KVQ_OK;
 }
 
 kvq_status kvq_get_device_error(kvq_cache* c, kvq_stream stream) {

@@ -75,6 +75,14 @@ cudaError_t launch_calibrate(const Geometry& g, const void* k, const void* v, in
                              unsigned* amax_scratch, float* scale, float* recip,
                              cudaStream_t stream);
 
+// Extend attention (kvq_extend.cu): one pass over each sequence's K/V tiles per
+// 64 (query, q head) rows of a kv head; no workspace.
+cudaError_t launch_extend(const Geometry& g, const LayerView& L, const void* q, int num_q_heads,
+                          int num_q_tokens, const int32_t* q_seq, const int32_t* q_len,
+                          const int32_t* page_table, int num_seqs, int max_pages_per_seq,
+                          float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
+                          void* out, int* err, cudaStream_t stream);
+
 // Decode attention plan: how many warp workers and how much workspace.
 struct DecodePlan {
   int group;          // q heads per kv head (G)

@@ -64,18 +64,29 @@ def test_extend_70b_shape_random_positions(kvq, orc, cuda, fmt):
     assert_attention_close(got, ref, f"{fmt} extend 70B")
 
 
-def test_extend_last_token_is_decode(kvq, cuda):
-    """One query per sequence at its last position is exactly a decode call."""
-    wl = synth.make_workload("ext_dec", "nvfp4", Hq=16, Hkv=2, seq_lens=[500, 77, 0, 33], seed=4)
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp4_mx_block16"])
+def test_extend_last_token_matches_decode(kvq, orc, cuda, fmt):
+    """One query per sequence at its last position is a decode: extend and
+    decode agree with the oracle (and with each other) within the tolerance."""
+    wl = synth.make_workload(f"ext_dec_{fmt}", fmt, Hq=16, Hkv=2, seq_lens=[500, 77, 0, 33], seed=4)
     c = gpu_cache_for(kvq, wl)
     store_layer(c, wl)
     q = bits_to_cuda(wl.q())
     pt = torch.from_numpy(wl.page_table).cuda()
-    dec = c.decode_attention(0, q, pt, torch.from_numpy(wl.seq_lens).cuda(), wl.sm_scale)
-    ext = c.extend_attention(0, q, torch.arange(wl.B, dtype=torch.int32, device="cuda"),
-                             torch.from_numpy(wl.seq_lens).cuda(), pt, wl.sm_scale)
+    sl = torch.from_numpy(wl.seq_lens).cuda()
+    dec = c.decode_attention(0, q, pt, sl, wl.sm_scale)
+    ext = c.extend_attention(0, q, torch.arange(wl.B, dtype=torch.int32, device="cuda"), sl, pt,
+                             wl.sm_scale)
     torch.cuda.synchronize()
-    assert torch.equal(dec.view(torch.int16), ext.view(torch.int16))
+    assert c.device_error() == 0
+    d = synth.bf16_bits_to_float(cuda_to_bits(dec)).astype(np.float64)
+    e = synth.bf16_bits_to_float(cuda_to_bits(ext)).astype(np.float64)
+    ref, rc = oracle_cache_for(orc, wl).decode_attention(wl.q(), wl.page_table, wl.seq_lens,
+                                                         wl.sm_scale)
+    assert rc == 0
+    assert_attention_close(d, ref, "decode")
+    assert_attention_close(e, ref, "extend")
+    assert (e[2] == 0).all()
 
 
 def test_extend_bad_rows_and_lengths(kvq, cuda):
