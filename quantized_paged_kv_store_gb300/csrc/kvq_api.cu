@@ -479,13 +479,10 @@ size_t kvq_decode_workspace_size(const kvq_cache* c, int batch, int num_q_heads,
   return plan.ws_bytes;
 }
 
-// Decode attention of `batch` queries; pt_rows (extend attention) names the
-// page-table row of each query, else query b reads row b.
-static kvq_status attention_common(kvq_cache* c, int layer, const void* q_bf16, int num_q_heads,
-                                   const int32_t* page_table, int max_pages_per_seq,
-                                   const int32_t* seq_lens, int batch, const int32_t* pt_rows,
-                                   int pt_nrows, float sm_scale, void* out_bf16, void* workspace,
-                                   size_t workspace_bytes, kvq_stream stream) {
+kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q_bf16, int num_q_heads,
+                                const int32_t* page_table, int max_pages_per_seq,
+                                const int32_t* seq_lens, int batch, float sm_scale, void* out_bf16,
+                                void* workspace, size_t workspace_bytes, kvq_stream stream) {
   kvq_status st = check_layer(c, layer);
   if (st) return st;
   if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0)
@@ -507,18 +504,10 @@ static kvq_status attention_common(kvq_cache* c, int layer, const void* q_bf16, 
   tensor_scales(c, layer, &kf, &vf);
   cudaError_t e = kvq::launch_decode(c->geo, view(c, layer), plan, q_bf16, num_q_heads, page_table,
                                      max_pages_per_seq, seq_lens, batch, sm_scale, kf, vf,
-                                     head_scales(c, layer), pt_rows, pt_nrows, out_bf16, workspace,
-                                     c->err, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+                                     head_scales(c, layer), nullptr, 0, out_bf16, workspace, c->err,
+                                     (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   return KVQ_OK;
-}
-
-kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q_bf16, int num_q_heads,
-                                const int32_t* page_table, int max_pages_per_seq,
-                                const int32_t* seq_lens, int batch, float sm_scale, void* out_bf16,
-                                void* workspace, size_t workspace_bytes, kvq_stream stream) {
-  return attention_common(c, layer, q_bf16, num_q_heads, page_table, max_pages_per_seq, seq_lens,
-                          batch, nullptr, 0, sm_scale, out_bf16, workspace, workspace_bytes, stream);
 }
 
 kvq_status kvq_extend_attention(kvq_cache* c, int layer, const void* q_bf16, int num_q_heads,
