@@ -159,3 +159,27 @@ def test_extend_attention_matches_torch_causal_sdpa(orc, fmt):
                                                                scale=wl.sm_scale, enable_gqa=True)
         np.testing.assert_allclose(out[i0:i0 + n], ref[0].permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
         i0 += n
+
+
+def test_extend_attention_arbitrary_positions(orc):
+    """Queries at arbitrary positions of interleaved sequences: each equals
+    PyTorch's SDPA over exactly its own prefix (no mask needed)."""
+    fmt = "nvfp4"
+    wl = synth.make_workload("xa", fmt, Hq=8, Hkv=2, D=32, seq_lens=[40, 23, 9], seed=17)
+    c = _store_all(orc, wl)
+    rng = np.random.default_rng(3)
+    q_seq = rng.integers(0, wl.B, 12).astype(np.int32)
+    q_len = np.array([rng.integers(0, int(wl.seq_lens[b]) + 1) for b in q_seq], np.int32)
+    q = synth.to_bf16_bits(torch.randn(12, wl.Hq, wl.D, generator=torch.Generator().manual_seed(8)))
+    out, rc = c.extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
+    assert rc == 0
+    qd = torch.from_numpy(q.view(np.int16).copy()).view(torch.bfloat16).double()
+    for i, (b, T) in enumerate(zip(q_seq, q_len)):
+        if T == 0:
+            assert (out[i] == 0).all()
+            continue
+        K = _exact_kv(fmt, c, wl, int(b), "k")[:T].permute(1, 0, 2)[None]
+        V = _exact_kv(fmt, c, wl, int(b), "v")[:T].permute(1, 0, 2)[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qd[i][None, :, None, :], K, V,
+                                                               scale=wl.sm_scale, enable_gqa=True)
+        np.testing.assert_allclose(out[i], ref[0, :, 0, :].numpy(), rtol=1e-12, atol=1e-12)
