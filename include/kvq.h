@@ -153,7 +153,9 @@ kvq_status kvq_quantize_and_store_per_head(kvq_cache* cache, int layer, const vo
  * scale = amax / M over the finite values (per tensor or per kv head), fp32
  * division, M = 448 (E4M3), 57344 (E5M2), 6 * 448 = 2688 (NVFP4 global scale:
  * the largest block scale lands on the E4M3 maximum); amax == 0 gives 1.0.
- * Stream-ordered, no host synchronization, no allocation.  Only valid on a
+ * Stream-ordered, no host synchronization, no allocation; every layer has its
+ * own reduction scratch, so calibrations of different layers may run on
+ * different streams at the same time.  Only valid on a
  * layer whose scales are not fixed yet (else KVQ_ERR_SCALE_MISMATCH); for bf16
  * and fp4_mx_block16 it fixes nothing but marks the layer as set.  Later
  * stores of the layer pass scales == NULL to kvq_quantize_and_store (explicit

@@ -33,7 +33,7 @@ struct kvq_cache {
   std::vector<char> uniform;    // [layers] every head has the same scales (mode kHost)
   float* dscale;                // [layers][2][kv_heads] device copy
   float* drecip;                // [layers][2][kv_heads] 1 / scale
-  unsigned* damax;              // [2][kv_heads] calibration scratch
+  unsigned* damax;              // [layers][2][kv_heads] calibration scratch (one slice per layer)
 };
 
 namespace {
@@ -271,7 +271,7 @@ kvq_status kvq_create_cache(kvq_format fmt, int layers, int kv_heads, int head_d
   const size_t ldb = (rows * g.data_row + 255) & ~(size_t)255;
   const size_t lsb = (rows * g.scale_row + 255) & ~(size_t)255;
   const size_t scale_bytes = ((size_t)layers * 2 * kv_heads * sizeof(float) + 255) & ~(size_t)255;
-  const size_t amax_bytes = (2 * (size_t)kv_heads * sizeof(unsigned) + 255) & ~(size_t)255;
+  const size_t amax_bytes = ((size_t)layers * 2 * kv_heads * sizeof(unsigned) + 255) & ~(size_t)255;
   const size_t pools = (2 * ldb + 2 * lsb) * (size_t)layers;
   const size_t total = pools + 2 * scale_bytes + amax_bytes + 256;
 
@@ -439,8 +439,9 @@ kvq_status kvq_calibrate_scales(kvq_cache* c, int layer, const void* k_bf16, con
     return KVQ_OK;
   }
   const size_t base = (size_t)layer * 2 * c->geo.kv_heads;
-  cudaError_t e = kvq::launch_calibrate(c->geo, k_bf16, v_bf16, num_tokens, per_head != 0, c->damax,
-                                        c->dscale + base, c->drecip + base, (cudaStream_t)stream);
+  cudaError_t e = kvq::launch_calibrate(c->geo, k_bf16, v_bf16, num_tokens, per_head != 0,
+                                        c->damax + base, c->dscale + base, c->drecip + base,
+                                        (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "calibration launch");
   c->mode[layer] = kDevice;
   return KVQ_OK;

@@ -43,6 +43,10 @@
 #include "kvq_internal.h"
 
 #include <algorithm>
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
 #include <type_traits>
 
 namespace kvq {
@@ -51,6 +55,7 @@ namespace {
 constexpr int kWarpsPerCta = 4;
 constexpr int kPidWin = 30;    // page ids prefetched per window (a multiple of every stage size)
 constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before giving up (~1 s)
+constexpr uint32_t kFaultWaitLimit = 64;   // polls of the injected never-completing wait
 
 template <kvq_format F>
 struct Traits {
@@ -64,7 +69,9 @@ struct Traits {
   static constexpr int kStage = kTps * kTileBytes;
   static constexpr int kStages = (F == KVQ_BF16) ? 3 : 2;
   static constexpr int kWarpSmem = kStages * kStage;
-  static constexpr int kCtaSmem = kWarpsPerCta * (kWarpSmem + kStages * 8);
+  // per warp: the stage ring, one mbarrier per stage and one that is never
+  // armed (the target of the injected wait of the failure-detection test)
+  static constexpr int kCtaSmem = kWarpsPerCta * (kWarpSmem + (kStages + 1) * 8);
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -152,7 +159,7 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 struct Ring {
   const uint8_t* gsmem;  // generic address of stage 0
   uint32_t smem;         // shared address of stage 0
-  uint32_t bar;          // shared address of the first mbarrier
+  uint32_t bar;          // shared address of the first mbarrier (one per stage, then `never`)
   uint32_t pos;          // stages consumed by this warp (monotonic)
   uint32_t issued;       // stages issued by this warp (monotonic)
   uint32_t dead_pos;     // first stage whose wait ran out
@@ -564,9 +571,16 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
     const uint32_t st = ring.pos % S;
     const uint32_t parity = (ring.pos / S) & 1u;
     if (!ring.dead) {
+      // The failure-detection test makes a warp's first wait target the
+      // mbarrier that is never armed, with a short limit, so that it runs out
+      // while the warp's first copies are in flight (they land in the drain).
+      const bool inject = a.fault_wait && ring.pos == 0;
+      const uint32_t wbar = inject ? ring.bar + 8 * S : ring.bar + 8 * st;
+      const uint32_t wpar = inject ? 0u : parity;
+      const uint32_t limit = inject ? kFaultWaitLimit : kWaitLimit;
       uint32_t polls = 0;
-      bool ok = mbar_try_wait(ring.bar + 8 * st, parity);
-      while (!ok && ++polls < kWaitLimit) ok = mbar_try_wait(ring.bar + 8 * st, parity);
+      bool ok = mbar_try_wait(wbar, wpar);
+      while (!ok && ++polls < limit) ok = mbar_try_wait(wbar, wpar);
       if (!__all_sync(0xffffffffu, ok)) {
         ring.dead = true;
         ring.dead_pos = ring.pos;
@@ -719,12 +733,12 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs
   ring.gsmem = smem_raw + warp * Tr::kWarpSmem;
   ring.smem = smem_addr(smem_raw) + warp * Tr::kWarpSmem;
   ring.dead_pos = 0;
-  ring.bar = smem_addr(smem_raw) + kWarpsPerCta * Tr::kWarpSmem + warp * Tr::kStages * 8;
+  ring.bar = smem_addr(smem_raw) + kWarpsPerCta * Tr::kWarpSmem + warp * (Tr::kStages + 1) * 8;
   ring.pos = 0;
   ring.issued = 0;
   ring.dead = false;
   if (lane == 0) {
-    for (int s = 0; s < Tr::kStages; ++s) mbar_init(ring.bar + 8 * s, 1);
+    for (int s = 0; s <= Tr::kStages; ++s) mbar_init(ring.bar + 8 * s, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
   }
@@ -819,30 +833,51 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+constexpr int kMaxDevices = 64;
+
+// Kernel attributes are per device: the dynamic shared-memory opt-in and the
+// occupancy query run once for each (format, device), with that device
+// current, under a lock; later calls read the cached CTA count.
 template <kvq_format F>
-cudaError_t prepare(int* ctas_per_sm) {
-  static int cached = 0;
-  if (!cached) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Traits<F>::kCtaSmem);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<F>, kWarpsPerCta * 32,
-                                                      Traits<F>::kCtaSmem);
-    if (e != cudaSuccess) return e;
-    cached = std::max(n, 1);
+cudaError_t prepare(int device, int* ctas_per_sm) {
+  static std::mutex mu;
+  static std::atomic<int> cached[kMaxDevices];
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  int n = cached[device].load(std::memory_order_acquire);
+  if (n == 0) {
+    std::lock_guard<std::mutex> lock(mu);
+    n = cached[device].load(std::memory_order_relaxed);
+    if (n == 0) {
+      int prev = -1;
+      cudaError_t e = cudaGetDevice(&prev);
+      if (e != cudaSuccess) return e;
+      if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(decode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Traits<F>::kCtaSmem);
+      int occ = 0;
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<F>, kWarpsPerCta * 32,
+                                                          Traits<F>::kCtaSmem);
+      if (prev != device) {
+        const cudaError_t e2 = cudaSetDevice(prev);
+        if (e == cudaSuccess) e = e2;
+      }
+      if (e != cudaSuccess) return e;
+      n = std::max(occ, 1);
+      cached[device].store(n, std::memory_order_release);
+    }
   }
-  *ctas_per_sm = cached;
+  *ctas_per_sm = n;
   return cudaSuccess;
 }
 
-cudaError_t ctas_per_sm(kvq_format f, int* n) {
+cudaError_t ctas_per_sm(kvq_format f, int device, int* n) {
   switch (f) {
-    case KVQ_BF16: return prepare<KVQ_BF16>(n);
-    case KVQ_FP8_E4M3: return prepare<KVQ_FP8_E4M3>(n);
-    case KVQ_FP8_E5M2: return prepare<KVQ_FP8_E5M2>(n);
-    case KVQ_FP4_BLOCK16: return prepare<KVQ_FP4_BLOCK16>(n);
-    case KVQ_NVFP4: return prepare<KVQ_NVFP4>(n);
+    case KVQ_BF16: return prepare<KVQ_BF16>(device, n);
+    case KVQ_FP8_E4M3: return prepare<KVQ_FP8_E4M3>(device, n);
+    case KVQ_FP8_E5M2: return prepare<KVQ_FP8_E5M2>(device, n);
+    case KVQ_FP4_BLOCK16: return prepare<KVQ_FP4_BLOCK16>(device, n);
+    case KVQ_NVFP4: return prepare<KVQ_NVFP4>(device, n);
   }
   return cudaErrorInvalidValue;
 }
@@ -871,7 +906,7 @@ bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_pe
     *why = "cannot query the SM count";
     return false;
   }
-  if (ctas_per_sm(g.fmt, &per_sm) != cudaSuccess) {
+  if (ctas_per_sm(g.fmt, device, &per_sm) != cudaSuccess) {
     *why = "cannot configure the decode kernel";
     return false;
   }
@@ -933,6 +968,10 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
   a.pt_rows = pt_rows;
   a.pt_nrows = pt_nrows;
   a.err = err;
+  // KVQ_FAULT=wait (failure-detection tests only): every warp's first stage
+  // wait gives up, the kernel reports KVQ_ERR_TIMEOUT and zeroes the outputs
+  const char* fault = std::getenv("KVQ_FAULT");
+  a.fault_wait = fault && std::strcmp(fault, "wait") == 0;
   if (batch == 0) return cudaSuccess;
   cudaError_t e = cudaErrorInvalidValue;
   switch (g.fmt) {

@@ -33,6 +33,7 @@ struct DecodeArgs {
   const float* vfac;  // per-kv-head V scales (or null)
   const int32_t* pt_rows;  // extend: page-table row of each query token b (or null: row b)
   int pt_nrows;            // rows of the page table when pt_rows is set
+  int fault_wait;          // failure-detection test: each warp's first stage wait runs out
 };
 
 

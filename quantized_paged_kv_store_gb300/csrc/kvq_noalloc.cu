@@ -53,11 +53,15 @@ extern "C" kvq_status kvq_decode_attention_noalloc(kvq_cache* cache, int layer, 
                                                    int max_pages_per_seq, const int32_t* seq_lens,
                                                    int batch, float sm_scale, void* out_bf16,
                                                    kvq_stream stream) {
-  if (!cache) return kvq_decode_attention(cache, layer, q_bf16, num_q_heads, page_table,
-                                          max_pages_per_seq, seq_lens, batch, sm_scale, out_bf16,
-                                          nullptr, 0, stream);  // reports the NULL cache
-  const size_t need = kvq_decode_workspace_size(cache, batch, num_q_heads, max_pages_per_seq);
-  if (need == 0) return KVQ_ERR_UNSUPPORTED;  // message already set
+  // A NULL cache, invalid sizes (INVALID_ARG) or an unsupported shape
+  // (UNSUPPORTED) leave no workspace size; the workspace entry point, called
+  // without one, validates the same arguments in the same order and returns
+  // that status and message before any device work.
+  const size_t need =
+      cache ? kvq_decode_workspace_size(cache, batch, num_q_heads, max_pages_per_seq) : 0;
+  if (need == 0)
+    return kvq_decode_attention(cache, layer, q_bf16, num_q_heads, page_table, max_pages_per_seq,
+                                seq_lens, batch, sm_scale, out_bf16, nullptr, 0, stream);
   if (need > kNoAllocScratchBytes) {
     kvq::set_error_message("kvq_decode_attention_noalloc: these sizes need %zu bytes of scratch, "
                           "more than its static %zu-byte array; use kvq_decode_attention with a "

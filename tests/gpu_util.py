@@ -32,15 +32,16 @@ def gpu_cache_for(kvq, wl, layers=None):
 
 
 def store_layer(cache, wl, layer=0, seqs=None, chunk=None):
-    """Quantize-and-store every token of the given sequences on the GPU."""
+    """Quantize-and-store every token of the given sequences on the GPU (the
+    layer's rows are drawn once; the same draws fix its scale inputs)."""
+    ks, vs = wl.kv_all(layer)
     s = wl.scales(layer)
     for b in (range(wl.B) if seqs is None else seqs):
         T = int(wl.seq_lens[b])
         step = chunk or max(T, 1)
         for t0 in range(0, T, step):
             t1 = min(T, t0 + step)
-            k, v = wl.kv(layer, b, t0, t1)
-            cache.quantize_and_store(layer, bits_to_cuda(k), bits_to_cuda(v),
+            cache.quantize_and_store(layer, bits_to_cuda(ks[b][t0:t1]), bits_to_cuda(vs[b][t0:t1]),
                                      torch.from_numpy(wl.slots(b, t0, t1)).cuda(), list(s))
 
 

@@ -50,3 +50,11 @@ def test_create_cache_rejects_bad_arguments_before_device_work(kvq):
         with pytest.raises(kvq.KVQError) as e:
             kvq.kvq_create_cache(*args)
         assert e.value.code == "KVQ_ERR_INVALID_ARG"
+
+
+def test_noalloc_null_cache_is_an_invalid_argument(kvq):
+    """The allocation-free decode entry point reports a NULL cache as
+    KVQ_ERR_INVALID_ARG before touching the device (no GPU needed)."""
+    st = kvq.lib.kvq_decode_attention_noalloc(None, 0, None, 64, None, 4, None, 2, 0.1, None, None)
+    assert kvq._binding._STATUS[st] == "KVQ_ERR_INVALID_ARG"
+    assert "NULL" in kvq.kvq_last_error_string()

@@ -86,6 +86,51 @@ def test_cfg4_nvfp4_32k_full_size_sampled(kvq, orc, cuda):
     assert_attention_close(got, ref, "cfg4 sampled")
 
 
+@pytest.mark.parametrize("fmt,B", [("bf16", 8), ("fp8_e4m3", 8), ("fp8_e5m2", 8),
+                                   ("fp4_mx_block16", 8), ("fp8_e4m3", 32),
+                                   ("fp4_mx_block16", 32)])
+def test_32k_full_size_sampled(kvq, orc, cuda, fmt, B):
+    """70B layer (Hq 64, Hkv 8) at 32K context, in the launch configuration the
+    benchmark times: with 8 sequences every warp worker of the persistent grid
+    gets 54 to 108 tiles (215 and more at 32 sequences), so each segment runs
+    past several 30-tile page-id windows and long stage chains (and, for FP4
+    block-16, long running V reference-exponent chains).  Three sequences, all
+    q heads, element by element against the oracle."""
+    wl = synth.cfg5_sweep_cell(fmt, 32768, B)
+    seqs = [0, B // 2 - 1, B - 1]
+    got, ref = _run(kvq, orc, wl, seqs=seqs)
+    assert_attention_close(got, ref, f"{fmt} 32K x {B} sampled")
+
+
+def test_cfg3_fp4_block16_16k_full_size_sampled(kvq, orc, cuda):
+    """The FP4 block-16 workload (70B layer, batch 8 at 16K), two sequences."""
+    wl = synth.cfg3_fp4b16_70b()
+    seqs = [1, 6]
+    got, ref = _run(kvq, orc, wl, seqs=seqs)
+    assert_attention_close(got, ref, "cfg3 sampled")
+
+
+def test_decode_bounded_wait_reports_timeout(kvq, cuda, monkeypatch):
+    """Failure detection without a fault: with KVQ_FAULT=wait every warp's first
+    stage wait targets an mbarrier that is never armed and gives up after a
+    short limit.  The kernel stops issuing copies, lets the ones in flight land
+    (bounded drain), reports KVQ_ERR_TIMEOUT and zeroes every output it could
+    not compute; the next call on the same cache is correct again."""
+    wl = synth.make_workload("tmo", "nvfp4", Hq=16, Hkv=2, seq_lens=[700, 300, 0, 64], seed=5)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    good = gpu_decode(c, wl)
+    assert c.device_error() == 0
+    monkeypatch.setenv("KVQ_FAULT", "wait")
+    got = gpu_decode(c, wl)
+    assert c.device_error() == kvq._binding._STATUS_CODES["KVQ_ERR_TIMEOUT"]
+    assert (got == 0).all()
+    monkeypatch.delenv("KVQ_FAULT")
+    again = gpu_decode(c, wl)
+    assert c.device_error() == 0
+    assert np.array_equal(again, good)
+
+
 def test_decode_bad_page_and_length(kvq, cuda):
     wl = synth.make_workload("bad", "fp8_e4m3", Hq=8, Hkv=2, seq_lens=[40, 40, 40], seed=2)
     c = gpu_cache_for(kvq, wl)

@@ -62,3 +62,19 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(kvq, cuda):
     with pytest.raises(kvq.KVQError) as e:
         kvq.kvq_decode_attention_noalloc(c.handle, 0, q, pt, sl, 0.1, out)
     assert e.value.code == "KVQ_ERR_UNSUPPORTED" and "static" in str(e.value)
+
+
+def test_noalloc_reports_invalid_arguments_as_the_workspace_call_does(kvq, cuda):
+    """Bad sizes give KVQ_ERR_INVALID_ARG and an unsupported shape gives
+    KVQ_ERR_UNSUPPORTED, exactly as kvq_decode_attention reports them."""
+    c = kvq.KVQCache("fp8_e4m3", 1, 8, 128, 16, 64)
+    q = torch.zeros(2, 64, 128, dtype=torch.bfloat16, device="cuda")
+    pt = torch.zeros(2, 4, dtype=torch.int32, device="cuda")
+    sl = torch.zeros(2, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    st = kvq.lib.kvq_decode_attention_noalloc(c.handle, 0, q.data_ptr(), 64, pt.data_ptr(), 4,
+                                              sl.data_ptr(), -1, 0.1, out.data_ptr(), None)
+    assert kvq._binding._STATUS[st] == "KVQ_ERR_INVALID_ARG"
+    st = kvq.lib.kvq_decode_attention_noalloc(c.handle, 0, q.data_ptr(), 8 * 17, pt.data_ptr(), 4,
+                                              sl.data_ptr(), 2, 0.1, out.data_ptr(), None)
+    assert kvq._binding._STATUS[st] == "KVQ_ERR_UNSUPPORTED"
