@@ -66,6 +66,11 @@ def parse_args(argv=None):
                    help="run only the --store measurement (no decode line)")
     p.add_argument("--next", default=None, help="time the per-head-scale decode, on-device "
                    "calibration and extend attention paths, one JSON line each appended to this file")
+    p.add_argument("--quant-error", default=None, help="report the quantization error of every "
+                   "format on the specified workloads (sampled sequences, GPU output against fp64 "
+                   "attention over the unquantized bf16 K/V), one JSON line each appended to this file")
+    p.add_argument("--no-per-format", action="store_true",
+                   help="skip the per-format decode timings of the bench workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=32,
@@ -218,6 +223,53 @@ def make_workload(fmt, seed, T=None, B=None):
     return synth.cfg5_sweep_cell(fmt, T, B, seed=seed)
 
 
+# ------------------------------------------------- quantization error (no oracle)
+def exact_attention_fp64(wl, ks, vs, seqs, q_bits):
+    """fp64 attention of the given sequences over their UNQUANTIZED bf16 K/V
+    (plain torch matmul/softmax, q head j reads kv head j // G): the answer an
+    unquantized cache would give, against which the quantized formats' outputs
+    are compared.  Returns {b: float64 [Hq][D]}."""
+    import numpy as np
+    import torch
+    import synth
+    G = wl.Hq // wl.Hkv
+    out = {}
+    for b in seqs:
+        q = torch.from_numpy(synth.bf16_bits_to_float(q_bits[b]).astype(np.float64))  # [Hq][D]
+        K = torch.from_numpy(synth.bf16_bits_to_float(ks[b]).astype(np.float64))    # [T][Hkv][D]
+        V = torch.from_numpy(synth.bf16_bits_to_float(vs[b]).astype(np.float64))
+        o = torch.zeros(wl.Hq, wl.D, dtype=torch.float64)
+        if K.shape[0] > 0:
+            for h in range(wl.Hkv):
+                z = (q[h * G:(h + 1) * G] @ K[:, h].T) * wl.sm_scale
+                o[h * G:(h + 1) * G] = torch.softmax(z, dim=-1) @ V[:, h]
+        out[b] = o.numpy()
+    return out
+
+
+def quant_error(got_rows, exact):
+    """Per (sequence, q head) relative L2 error of an attention output against
+    the exact unquantized answer: max and mean over the sampled rows, and the
+    largest elementwise error."""
+    import numpy as np
+    rel, ab = [], 0.0
+    for b, ref in exact.items():
+        g = got_rows[b]
+        den = np.linalg.norm(ref, axis=-1)
+        num = np.linalg.norm(g - ref, axis=-1)
+        rel.extend(list(np.where(den > 0, num / np.where(den > 0, den, 1), num)))
+        ab = max(ab, float(np.abs(g - ref).max()))
+    return {"max_rel_l2": float(np.max(rel)), "mean_rel_l2": float(np.mean(rel)), "max_abs": ab,
+            "rows": len(rel)}
+
+
+def out_rows(d_out, seqs):
+    import numpy as np
+    import synth
+    bits = d_out.contiguous().view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+    return {b: synth.bf16_bits_to_float(bits[b]).astype(np.float64) for b in seqs}
+
+
 # --------------------------------------------------------------- oracle timing
 def oracle_time(wl, seqs, ks, vs, reps=1):
     """Seconds the CPU oracle takes to run decode attention for `seqs` (after
@@ -238,8 +290,92 @@ def oracle_time(wl, seqs, ks, vs, reps=1):
     return dt, nbytes, oracle.num_threads()
 
 
+def oracle_store_time(n_tokens, seed):
+    """Seconds the CPU oracle takes to quantize-and-store an n_tokens prefix of
+    one sequence of the FP4 block-16 prefill workload (70B layer, 16K), and the
+    algorithmic bytes (bf16 K and V read, cache rows and scales written, slot ids)."""
+    import oracle
+    import synth
+    wl = synth.cfg3_fp4b16_70b(seed=seed)
+    k, v = wl.kv(0, 0, 0, n_tokens)
+    c = oracle.OracleCache(wl.fmt, wl.Hkv, wl.D, wl.P, wl.num_pages)
+    slots = wl.slots(0, 0, n_tokens)
+    t0 = time.perf_counter()
+    c.quantize_store(k, v, slots, None)
+    dt = time.perf_counter() - t0
+    nbytes = n_tokens * wl.Hkv * (2 * wl.D * 2 + 2 * (wl.D // 2 + wl.D // 16)) + n_tokens * 8
+    return dt, nbytes
+
+
+def cpu_baseline(wl, ks, vs, seed):
+    """The oracle as it stands, on this host's cores: fp64 decode attention of a
+    sample of the bench workload (all cores and one thread) and quantize-and-store
+    of a sample of the FP4 block-16 prefill (all cores and one thread)."""
+    import oracle
+    cores = oracle.num_threads()
+    seqs = list(range(min(4, wl.B)))
+    dt, nb, _ = oracle_time(wl, seqs, ks, vs)
+    # one thread: one sequence
+    oracle.set_num_threads(1)
+    try:
+        dt1, nb1, _ = oracle_time(wl, [0], ks, vs)
+        st1, sb1 = oracle_store_time(2048, seed)
+    finally:
+        oracle.set_num_threads(cores)
+    st, sb = oracle_store_time(8192, seed)
+    ntok = sum(int(wl.seq_lens[b]) for b in seqs)
+    return {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle decode attention of sequences {seqs} ({ntok} tokens x "
+                      f"{wl.Hkv} kv heads, all {wl.Hq} q heads) of the same workload; {dt:.2f} s",
+            "single_thread": {"value": round(nb1 / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"sequence 0 ({int(wl.seq_lens[0])} tokens); {dt1:.2f} s"},
+            "store": {"value": round(sb / st / 1e9, 4), "unit": "GB/s", "cores": cores,
+                      "single_thread_value": round(sb1 / st1 / 1e9, 4),
+                      "sample": f"oracle quantize-and-store (fp4_mx_block16) of the first 8192 "
+                                f"(one thread: 2048) tokens of sequence 0 of the 70B-layer 16K x 8 "
+                                f"prefill; {st:.2f} s / {st1:.2f} s"}}
+
+
 # ------------------------------------------------------------------- our arm
-def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True):
+PER_FORMAT = ("nvfp4", "fp4_mx_block16", "fp8_e4m3", "fp8_e5m2", "bf16")
+
+
+def per_format_cells(args, wl, ks, vs, d_q, d_pt, d_sl, exact, dev, peak):
+    """Decode attention of the same workload (same K/V draws, every token
+    stored) in each cache format: mean CUDA-event time per call, algorithmic
+    GB/s and fraction of peak, and the quantization error of its output on the
+    sampled sequences."""
+    import numpy as np
+    import torch
+    import quantized_paged_kv_store_gb300 as kvq
+    kall = synth_to_cuda(np.concatenate(ks))
+    vall = synth_to_cuda(np.concatenate(vs))
+    slots = torch.from_numpy(np.concatenate([wl.slots(b) for b in range(wl.B)])).to(dev)
+    steps = max(20, min(args.steps, 200))
+    warm = max(3, min(args.warmup, 10))
+    cells = {}
+    for f in PER_FORMAT:
+        scales = [float(x) for x in wl.scales_for(f, ks, vs)]
+        cache = kvq.KVQCache(f, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
+        cache.quantize_and_store(0, kall, vall, slots, scales)
+        out = torch.empty_like(d_q)
+        ws = torch.empty(cache.workspace_size(wl.B, wl.Hq, wl.max_pages), dtype=torch.uint8, device=dev)
+        ms = _time_calls(lambda: cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale, out, ws),
+                         steps, warm)
+        if cache.device_error() != 0:
+            raise RuntimeError(f"device error in the {f} per-format decode")
+        nbytes = algorithmic_bytes(wl, f)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        cells[f] = {"ms_per_call": round(ms, 5), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                    "bytes_per_call": nbytes, "calls": steps,
+                    "quant_error": {k: (round(v, 6) if isinstance(v, float) else v)
+                                    for k, v in quant_error(out_rows(out, exact.keys()), exact).items()}}
+        cache.close()
+    del kall, vall
+    return cells
+
+
+def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True, with_extra=False):
     import numpy as np
     import torch
     import quantized_paged_kv_store_gb300 as kvq
@@ -343,15 +479,21 @@ def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True):
         res["e2e"] = {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke}
 
+    if with_extra and rank == 0:
+        # quantization error of the timed output against fp64 attention over the
+        # unquantized bf16 K/V of two sampled sequences (the longest and one more)
+        seqs_q = sorted({int(np.argmax(wl.seq_lens)), 3 % wl.B})
+        exact = exact_attention_fp64(wl, ks, vs, seqs_q, q_h)
+        qe = quant_error(out_rows(d_out, seqs_q), exact)
+        res["quant_error"] = {"format": fmt, "sequences": seqs_q,
+                              **{k: (round(v, 6) if isinstance(v, float) else v) for k, v in qe.items()},
+                              "reference": "fp64 attention over the unquantized bf16 K/V (plain torch)"}
+        if not args.no_per_format:
+            cache.close()
+            res["per_format"] = per_format_cells(args, wl, ks, vs, d_q, d_pt, d_sl, exact, dev,
+                                                 peak_hbm()[0])
     if with_cpu and rank == 0 and world == 1:
-        seqs = list(range(min(4, wl.B)))
-        dt, nb, cores = oracle_time(wl, seqs, ks, vs)
-        res["cpu_baseline"] = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
-                               "kind": "oracle",
-                               "sample": f"fp64 oracle decode attention of sequences {seqs} "
-                                         f"({sum(int(wl.seq_lens[b]) for b in seqs)} tokens x "
-                                         f"{wl.Hkv} kv heads, all {wl.Hq} q heads) of the same "
-                                         f"workload; {dt:.2f} s"}
+        res["cpu_baseline"] = cpu_baseline(wl, ks, vs, args.seed)
     cache.close()
     return res
 
@@ -366,7 +508,8 @@ def run_ours(args):
     import torch
     rank, world = dist_init("nccl")
     fmt = args.format
-    r = run_cell(args, fmt, with_cpu=not args.no_cpu_baseline, with_e2e=not args.no_e2e)
+    r = run_cell(args, fmt, with_cpu=not args.no_cpu_baseline, with_e2e=not args.no_e2e,
+                 with_extra=True)
     wl = r["wl"]
     peak, peak_kind = peak_hbm()
     achieved = r["decode_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
@@ -406,6 +549,10 @@ def run_ours(args):
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if "per_format" in r:
+        line["per_format"] = r["per_format"]
+    if "quant_error" in r:
+        line["quant_error"] = r["quant_error"]
     if "e2e" in r:
         line["e2e"] = r["e2e"]
     if "cpu_baseline" in r:
@@ -618,6 +765,55 @@ def run_next(args):
     return out
 
 
+def run_quant_error(args):
+    """Quantization error of every format on the specified workloads: for a few
+    sampled sequences of each, the GPU decode output of each cache format (all
+    q heads) against fp64 attention over the unquantized bf16 K/V.  Scale
+    inputs follow each workload's calibration recipe over all its sequences;
+    only the sampled sequences are stored and decoded (attention per sequence
+    does not depend on the others)."""
+    import numpy as np
+    import torch
+    import quantized_paged_kv_store_gb300 as kvq
+    import synth
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfgs = [("cfg1 E4M3 1 layer, Hq 32, Hkv 8, 2 x 256", synth.cfg1_e4m3_small(), [0, 1]),
+            ("cfg2 Llama-3-8B layer 0, Hq 32, Hkv 8, 8 x U[1K, 4K]",
+             synth.cfg2_llama8b_stack(layers=1), [0, 4, 7]),
+            ("cfg3 70B layer, 8 x 16K", synth.cfg3_fp4b16_70b(), [1, 6]),
+            ("cfg4 70B layer, 32 x U[24K, 32K]", synth.cfg4_nvfp4_70b_32k(), None)]
+    for name, wl, seqs in cfgs:
+        ks, vs = wl.kv_all(0)
+        if seqs is None:
+            seqs = sorted({int(np.argmax(wl.seq_lens)), 3})
+        q_h = wl.q(0)
+        exact = exact_attention_fp64(wl, ks, vs, seqs, q_h)
+        sub = np.asarray(seqs)
+        d_q = synth_to_cuda(q_h[sub])
+        d_pt = torch.from_numpy(np.ascontiguousarray(wl.page_table[sub])).to(dev)
+        d_sl = torch.from_numpy(np.ascontiguousarray(wl.seq_lens[sub])).to(dev)
+        for f in PER_FORMAT:
+            scales = [float(x) for x in wl.scales_for(f, ks, vs)]
+            cache = kvq.KVQCache(f, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
+            for b in seqs:
+                cache.quantize_and_store(0, synth_to_cuda(ks[b]), synth_to_cuda(vs[b]),
+                                         torch.from_numpy(wl.slots(b)).to(dev), scales)
+            out = cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale)
+            if cache.device_error() != 0:
+                raise RuntimeError(f"device error in the quantization-error run ({name}, {f})")
+            rows = out_rows(out, range(len(seqs)))
+            qe = quant_error({b: rows[i] for i, b in enumerate(seqs)}, exact)
+            with open(args.quant_error, "a") as fh:
+                fh.write(json.dumps({"workload": name, "format": f, "sequences": seqs,
+                                     "tokens": [int(wl.seq_lens[b]) for b in seqs],
+                                     "scales": scales, **qe}) + "\n")
+            cache.close()
+
+
 # ------------------------------------------------------------ reference arm
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is a bounded sample of the
@@ -682,6 +878,9 @@ def main(argv=None):
         return
     if args.next:
         run_next(args)
+        return
+    if args.quant_error:
+        run_quant_error(args)
         return
     if args.impl == "reference":
         run_reference(args)

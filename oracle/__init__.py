@@ -75,6 +75,8 @@ def _load():
             lib.orc_calibrate_scales.restype = i32
             lib.orc_num_threads.argtypes = []
             lib.orc_num_threads.restype = i32
+            lib.orc_set_num_threads.argtypes = [i32]
+            lib.orc_set_num_threads.restype = i32
             _lib = lib
     return _lib
 
@@ -131,6 +133,11 @@ def bytes_per_token(fmt, layers: int, kv_heads: int, head_dim: int) -> int:
 
 def num_threads() -> int:
     return _load().orc_num_threads()
+
+
+def set_num_threads(n: int) -> int:
+    """OpenMP threads of later oracle calls; returns the count in effect."""
+    return _load().orc_set_num_threads(int(n))
 
 
 def calibrate_scales(fmt, x_bf16: np.ndarray, per_head: bool) -> np.ndarray:

@@ -528,3 +528,14 @@ int orc_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Sets the OpenMP thread count of later calls (n >= 1), for single-thread
+ * timings of the baseline; returns the count now in effect. */
+int orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+  return orc_num_threads();
+}

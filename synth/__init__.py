@@ -144,16 +144,33 @@ class Workload:
             ks.append(k)
             vs.append(v)
         if layer not in self._scales:
-            self._scales[layer] = self._scales_from(ks, vs)
+            amax = self._scales.setdefault(("amax", layer), self._amax_of(ks, vs))
+            self._scales[layer] = self._scales_of(amax)
         return ks, vs
 
-    def _scales_from(self, ks, vs) -> np.ndarray:
-        div = _CAL_DIVISOR.get(self.fmt)
-        if div is None or self.scale_mode == "one":
-            return np.ones(2, np.float32)
+    def _scales_from(self, ks, vs, fmt=None) -> np.ndarray:
+        return self._scales_of(self._amax_of(ks, vs), fmt)
+
+    @staticmethod
+    def _amax_of(ks, vs):
         ka = max((float(np.abs(bf16_bits_to_float(k)).max()) for k in ks if k.size), default=0.0)
         va = max((float(np.abs(bf16_bits_to_float(v)).max()) for v in vs if v.size), default=0.0)
+        return ka, va
+
+    def _scales_of(self, amax, fmt=None) -> np.ndarray:
+        div = _CAL_DIVISOR.get(fmt or self.fmt)
+        if div is None or self.scale_mode == "one":
+            return np.ones(2, np.float32)
+        ka, va = amax
         return np.array([ka / div if ka > 0 else 1.0, va / div if va > 0 else 1.0], np.float32)
+
+    def scales_for(self, fmt: str, ks, vs, layer: int = 0) -> np.ndarray:
+        """The scale inputs the calibration recipe gives format `fmt` on this
+        layer's rows ks, vs (the per-tensor amax is computed once per layer)."""
+        key = ("amax", layer)
+        if key not in self._scales:
+            self._scales[key] = self._amax_of(ks, vs)
+        return self._scales_of(self._scales[key], fmt)
 
     def scales(self, layer: int = 0) -> np.ndarray:
         """float32 [2]: FP8 {k_scale, v_scale} or NVFP4 {g_k, g_v} = amax / format max,
