@@ -140,14 +140,28 @@ __device__ __forceinline__ uint32_t f32x2_to_bf2(float lo, float hi) {
 template <int K>
 __device__ __forceinline__ uint32_t e2m1_byte_h2(uint32_t x) { return dec2_e2m1_h2<K>(x); }
 
-// half2 of (2^da, 2^db) for da, db <= 0: exact down to 2^-24 (f16 subnormals
+// half2 of (2^da, 2^db) for da, db <= 15: exact down to 2^-24 (f16 subnormals
 // included), 0 below.  Built as fp32 powers of two (exponent field, clamped
 // at 2^-126) and rounded to f16 by one convert.
-__device__ __forceinline__ uint32_t h2_pow2_nonpos(int da, int db) {
+__device__ __forceinline__ uint32_t h2_pow2(int da, int db) {
   const float fa = __uint_as_float((uint32_t)(max(da, -126) + 127) << 23);
   const float fb = __uint_as_float((uint32_t)(max(db, -126) + 127) << 23);
   return f32x2_to_h2(fa, fb);
 }
+
+// FP4 block-16 factors without the fp32 route.  Two E8M0 codes b0, b1 held in
+// the halves of x (b0 | b1 << 16) and a reference code ref give
+//   y = x + (7 - ref) * 0x10001,  halves b - ref + 7
+// (one 32-bit add: with every half in [0, 15] no borrow or carry crosses the
+// halves).  y is "in window" iff (y & 0xFFF0FFF0) == 0, i.e. both codes lie in
+// [ref - 7, ref + 8]; a code outside makes its half >= 16 (an underflow leaves
+// 0xFFxx there).  In window, (y << 10) + 0x20002000 is the half2 of
+// (2^(b0 - ref), 2^(b1 - ref)): exponent field b - ref + 15, exact.
+__device__ __forceinline__ uint32_t e8m0_window(uint32_t x, int ref) {
+  return x + (uint32_t)(7 - ref) * 0x10001u;
+}
+__device__ __forceinline__ uint32_t e8m0_window_h2(uint32_t y) { return (y << 10) + 0x20002000u; }
+constexpr uint32_t kWindowMiss = 0xFFF0FFF0u;
 
 __device__ __forceinline__ int warp_sum_i(int v) {
 #pragma unroll
@@ -167,13 +181,14 @@ struct Ring {
 };
 
 // Logits of one 16-token tile: s = (K^ Q'^T) for rows r, r+8 and heads 2q,
-// 2q+1 (before the per-head scale); rs0/rs1 are the FP4 block-16 row factors.
+// 2q+1 (before the per-head scale).  FP4 block-16: kf holds the half2 block
+// factors 2^(E - kref) of (row r, block 2q), (r, 2q+1), (r+8, 2q), (r+8, 2q+1),
+// each broadcast to both halves; 2^kref is applied with the per-head scale.
 template <kvq_format F>
 __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, int r, int q,
-                                        const uint32_t (&qb)[8][2], float (&s)[4], float& rs0,
-                                        float& rs1) {
+                                        const uint32_t (&qb)[8][2], float (&s)[4],
+                                        const uint32_t (&kf)[4]) {
   s[0] = s[1] = s[2] = s[3] = 0.f;
-  rs0 = rs1 = 1.f;
   if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
     const uint4 x0 = lds128(sK + r * 128 + q * 32), x1 = lds128(sK + r * 128 + q * 32 + 16);
     const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
@@ -214,31 +229,20 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
   } else {
     const uint4 x = lds128(sK + r * 64 + q * 16);
     const uint4 y = lds128(sK + (r + 8) * 64 + q * 16);
-    const uint32_t sc0 = *reinterpret_cast<const uint16_t*>(sKs + r * 8 + 2 * q);
-    const uint32_t sc1 = *reinterpret_cast<const uint16_t*>(sKs + (r + 8) * 8 + 2 * q);
     uint32_t f00, f01, f10, f11;  // f16x2 factors: row r / r+8, block 2q / 2q+1
     if (F == KVQ_NVFP4) {
+      const uint32_t sc0 = *reinterpret_cast<const uint16_t*>(sKs + r * 8 + 2 * q);
+      const uint32_t sc1 = *reinterpret_cast<const uint16_t*>(sKs + (r + 8) * 8 + 2 * q);
       const uint32_t h0 = dec2_e4m3_h2(sc0), h1 = dec2_e4m3_h2(sc1);
       f00 = __byte_perm(h0, 0, 0x1010);
       f01 = __byte_perm(h0, 0, 0x3232);
       f10 = __byte_perm(h1, 0, 0x1010);
       f11 = __byte_perm(h1, 0, 0x3232);
     } else {
-      // row maximum exponent over the 8 blocks (4 lanes x 2 blocks)
-      int e0 = max((int)(sc0 & 0xFF), (int)(sc0 >> 8));
-      int e1 = max((int)(sc1 & 0xFF), (int)(sc1 >> 8));
-      e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 1));
-      e0 = max(e0, __shfl_xor_sync(0xffffffffu, e0, 2));
-      e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 1));
-      e1 = max(e1, __shfl_xor_sync(0xffffffffu, e1, 2));
-      const uint32_t h0 = h2_pow2_nonpos((int)(sc0 & 0xFF) - e0, (int)(sc0 >> 8) - e0);
-      const uint32_t h1 = h2_pow2_nonpos((int)(sc1 & 0xFF) - e1, (int)(sc1 >> 8) - e1);
-      f00 = __byte_perm(h0, 0, 0x1010);
-      f01 = __byte_perm(h0, 0, 0x3232);
-      f10 = __byte_perm(h1, 0, 0x1010);
-      f11 = __byte_perm(h1, 0, 0x3232);
-      rs0 = exp2i(e0 - 127);
-      rs1 = exp2i(e1 - 127);
+      f00 = kf[0];
+      f01 = kf[1];
+      f10 = kf[2];
+      f11 = kf[3];
     }
     const uint32_t kw[4] = {x.x, x.y, x.z, x.w}, kw8[4] = {y.x, y.y, y.z, y.w};
     float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: two independent MMA chains
@@ -373,11 +377,17 @@ __device__ __forceinline__ void tile_pv(const uint8_t* sV, const uint8_t* sVs, i
         fab = dec2_e4m3_h2(sa | (sb << 8));
         fcd = dec2_e4m3_h2(sc | (sd << 8));
       } else {
-        // running reference exponent of V block r over the tokens seen
-        int et = max(max((int)sa, (int)sb), max((int)sc, (int)sd));
-        et = max(et, __shfl_xor_sync(0xffffffffu, et, 1));
-        et = max(et, __shfl_xor_sync(0xffffffffu, et, 2));
-        if (__any_sync(0xffffffffu, et > vref)) {
+        // factors 2^(E - vref) against the running reference exponent of V
+        // block r (per lane quad): packed integer path while every code of
+        // the warp lies within [vref - 7, vref + 8]; otherwise raise the
+        // reference to the quad's maximum (rescaling the accumulator) and
+        // build the factors exactly through fp32
+        const uint32_t xab = __byte_perm(sa, sb, 0x5410), xcd = __byte_perm(sc, sd, 0x5410);
+        const uint32_t yab = e8m0_window(xab, vref), ycd = e8m0_window(xcd, vref);
+        if (__any_sync(0xffffffffu, ((yab | ycd) & kWindowMiss) != 0u)) {
+          int et = max(max((int)sa, (int)sb), max((int)sc, (int)sd));
+          et = max(et, __shfl_xor_sync(0xffffffffu, et, 1));
+          et = max(et, __shfl_xor_sync(0xffffffffu, et, 2));
           if (et > vref) {
             const float f = (vref < -127) ? 0.f : exp2i(vref - et);
 #pragma unroll
@@ -389,9 +399,12 @@ __device__ __forceinline__ void tile_pv(const uint8_t* sV, const uint8_t* sVs, i
             }
             vref = et;
           }
+          fab = h2_pow2((int)sa - vref, (int)sb - vref);
+          fcd = h2_pow2((int)sc - vref, (int)sd - vref);
+        } else {
+          fab = e8m0_window_h2(yab);
+          fcd = e8m0_window_h2(ycd);
         }
-        fab = h2_pow2_nonpos((int)sa - vref, (int)sb - vref);
-        fcd = h2_pow2_nonpos((int)sc - vref, (int)sd - vref);
       }
       // nibble pairs (token a | token b << 4) for even / odd nibble index
       const uint32_t ev0 = (A.x & 0x0F0F0F0Fu) | ((Bv.x << 4) & 0xF0F0F0F0u);
@@ -496,6 +509,8 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   int vref = -1000;  // FP4 block-16: reference exponent code of V block r
+  int kref = -1000;  // FP4 block-16: reference exponent code of the K tiles of a chunk
+  float kcs0 = cs0, kcs1 = cs1;  // per-head logit scales, times 2^(kref - 127) for FP4 block-16
   bool poison = false;
 
   // ---- page ids, prefetched one window (32 tiles) ahead ----------------------
@@ -567,20 +582,27 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
   if (!ring.dead)
     for (int c = 0; c < min(S, nch); ++c) issue(c);
 
+  // Failure-detection test: the warp's first wait targets the mbarrier that is
+  // never armed, with a short limit, so that it runs out while the warp's first
+  // copies are in flight (they land in the bounded drain at the kernel's end).
+  if (a.fault_wait && ring.pos == 0 && !ring.dead) {
+    uint32_t polls = 0;
+    bool ok = mbar_try_wait(ring.bar + 8 * S, 0u);
+    while (!ok && ++polls < kFaultWaitLimit) ok = mbar_try_wait(ring.bar + 8 * S, 0u);
+    if (!__all_sync(0xffffffffu, ok)) {
+      ring.dead = true;
+      ring.dead_pos = ring.pos;
+      if (lane == 0) atomicOr(a.err, kErrTimeout);
+    }
+  }
+
   for (int c = 0; c < nch; ++c) {
     const uint32_t st = ring.pos % S;
     const uint32_t parity = (ring.pos / S) & 1u;
     if (!ring.dead) {
-      // The failure-detection test makes a warp's first wait target the
-      // mbarrier that is never armed, with a short limit, so that it runs out
-      // while the warp's first copies are in flight (they land in the drain).
-      const bool inject = a.fault_wait && ring.pos == 0;
-      const uint32_t wbar = inject ? ring.bar + 8 * S : ring.bar + 8 * st;
-      const uint32_t wpar = inject ? 0u : parity;
-      const uint32_t limit = inject ? kFaultWaitLimit : kWaitLimit;
       uint32_t polls = 0;
-      bool ok = mbar_try_wait(wbar, wpar);
-      while (!ok && ++polls < limit) ok = mbar_try_wait(wbar, wpar);
+      bool ok = mbar_try_wait(ring.bar + 8 * st, parity);
+      while (!ok && ++polls < kWaitLimit) ok = mbar_try_wait(ring.bar + 8 * st, parity);
       if (!__all_sync(0xffffffffu, ok)) {
         ring.dead = true;
         ring.dead_pos = ring.pos;
@@ -601,26 +623,72 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
     auto run_chunk = [&](auto nt_const, auto full_const) {
       constexpr int NT = decltype(nt_const)::value;
       constexpr bool FULL = decltype(full_const)::value;
-      // ---- logits of the chunk's tiles ----
-      float sc[NT][4];
       int nvalid[NT];
+#pragma unroll
+      for (int tt = 0; tt < NT; ++tt)
+        nvalid[tt] = FULL ? kTile : min(kTile, T - (t0 + c * TPS + tt) * kTile);
+
+      // ---- logits of the chunk's tiles ----
+      // FP4 block-16: K block factors 2^(E - kref) against one reference code
+      // kref; the logits carry 2^(kref - 127) in the per-head scale kcs.  A
+      // tile whose codes all lie in kref's window [kref - 7, kref + 8] builds
+      // its factors with packed integer ops; otherwise kref is re-anchored at
+      // the tile's largest code (earlier tiles of the chunk are rescaled to
+      // it) and the tile's factors go through fp32 (exact down to 2^-24).
+      float sc[NT][4];
 #pragma unroll
       for (int tt = 0; tt < NT; ++tt) {
         const uint8_t* tb = stage + tt * Tr::kTileBytes;
-        float rs0, rs1;
-        tile_qk<F>(tb, tb + 2 * Tr::kData, r, q, qb, sc[tt], rs0, rs1);
-        if (F == KVQ_FP4_BLOCK16) {  // per-row 2^Emax factors
-          sc[tt][0] *= rs0;
-          sc[tt][1] *= rs0;
-          sc[tt][2] *= rs1;
-          sc[tt][3] *= rs1;
+        uint32_t kf[4] = {0u, 0u, 0u, 0u};
+        if constexpr (F == KVQ_FP4_BLOCK16) {
+          const uint8_t* ks = tb + 2 * Tr::kData;
+          uint32_t s0 = *reinterpret_cast<const uint16_t*>(ks + r * 8 + 2 * q);
+          uint32_t s1 = *reinterpret_cast<const uint16_t*>(ks + (r + 8) * 8 + 2 * q);
+          if (!FULL) {  // rows past the sequence end: no say in the reference
+            if (r >= nvalid[tt]) s0 = 0u;
+            if (r + 8 >= nvalid[tt]) s1 = 0u;
+          }
+          const uint32_t x0 = __byte_perm(s0, 0, 0x4140), x1 = __byte_perm(s1, 0, 0x4140);
+          uint32_t y0 = e8m0_window(x0, kref), y1 = e8m0_window(x1, kref);
+          uint32_t h0, h1;
+          if (__any_sync(0xffffffffu, ((y0 | y1) & kWindowMiss) != 0u)) {
+            const uint32_t m2 = __vmaxu2(x0, x1);
+            uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (kref >= 0) {  // earlier tiles of the chunk: to the new reference
+              // 2^(kref - mx) as two factors (the difference spans [-254, 254])
+              const int d = kref - (int)mx, d1 = max(-127, min(127, d));
+              const float g1 = exp2i(d1), g2 = exp2i(max(-127, min(127, d - d1)));
+#pragma unroll
+              for (int t2 = 0; t2 < tt; ++t2) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[t2][i] = (sc[t2][i] * g1) * g2;
+              }
+            }
+            kref = (int)mx;
+            const float f = exp2i(kref - 127);
+            kcs0 = cs0 * f;
+            kcs1 = cs1 * f;
+            h0 = h2_pow2((int)(x0 & 0xFFFFu) - kref, (int)(x0 >> 16) - kref);
+            h1 = h2_pow2((int)(x1 & 0xFFFFu) - kref, (int)(x1 >> 16) - kref);
+          } else {
+            h0 = e8m0_window_h2(y0);
+            h1 = e8m0_window_h2(y1);
+          }
+          kf[0] = __byte_perm(h0, 0, 0x1010);
+          kf[1] = __byte_perm(h0, 0, 0x3232);
+          kf[2] = __byte_perm(h1, 0, 0x1010);
+          kf[3] = __byte_perm(h1, 0, 0x3232);
         }
-        nvalid[tt] = FULL ? kTile : min(kTile, T - (t0 + c * TPS + tt) * kTile);
+        tile_qk<F>(tb, tb + 2 * Tr::kData, r, q, qb, sc[tt], kf);
         if (!FULL && nvalid[tt] < kTile) {
           if (r >= nvalid[tt]) sc[tt][0] = sc[tt][1] = -INFINITY;
           if (r + 8 >= nvalid[tt]) sc[tt][2] = sc[tt][3] = -INFINITY;
         }
       }
+      const float c0 = (F == KVQ_FP4_BLOCK16) ? kcs0 : cs0;
+      const float c1 = (F == KVQ_FP4_BLOCK16) ? kcs1 : cs1;
 
       // ---- online softmax on scaled logits cs * s (cs > 0), rescaling lazily ----
       float x0 = fmaxf(sc[0][0], sc[0][2]), x1 = fmaxf(sc[0][1], sc[0][3]);
@@ -629,8 +697,8 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         x0 = fmaxf(x0, fmaxf(sc[tt][0], sc[tt][2]));
         x1 = fmaxf(x1, fmaxf(sc[tt][1], sc[tt][3]));
       }
-      x0 *= cs0;
-      x1 *= cs1;
+      x0 *= c0;
+      x1 *= c1;
       if (__any_sync(0xffffffffu, x0 > m0 + kLazy || x1 > m1 + kLazy)) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -655,8 +723,8 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
       // ---- O^T += V^T P^T ----
 #pragma unroll
       for (int tt = 0; tt < NT; ++tt) {
-        const float p0 = ex2(fmaf(sc[tt][0], cs0, -m0)), p1 = ex2(fmaf(sc[tt][1], cs1, -m1));
-        const float p2 = ex2(fmaf(sc[tt][2], cs0, -m0)), p3 = ex2(fmaf(sc[tt][3], cs1, -m1));
+        const float p0 = ex2(fmaf(sc[tt][0], c0, -m0)), p1 = ex2(fmaf(sc[tt][1], c1, -m1));
+        const float p2 = ex2(fmaf(sc[tt][2], c0, -m0)), p3 = ex2(fmaf(sc[tt][3], c1, -m1));
         l0 += p0 + p2;
         l1 += p1 + p3;
         const uint8_t* tb = stage + tt * Tr::kTileBytes;

@@ -27,6 +27,8 @@ struct StoreArgs {
   uint8_t* scales[2];
   float s[2];            // FP8 scale / NVFP4 global scale per K, V
   float rs[2];           // FP8: 1 / s (IEEE)
+  float s6[2];           // NVFP4: RN(6 g), the block-scale divisor
+  float rs6[2];          // NVFP4: RN(1 / RN(6 g))
   const int64_t* slots;
   int64_t n;             // tokens
   int H, D, P;
@@ -42,15 +44,37 @@ struct StoreArgs {
 };
 
 // Largest bf16 magnitude of the 16 values as fp32 bits; NaN propagates, so
-// bits >= 0x7F800000 flags a non-finite block.
+// bits >= 0x7F800000 flags a non-finite block.  (max.xorsign.abs takes the
+// larger magnitude; the sign it sets is dropped at the end.)
 __device__ __forceinline__ uint32_t block_amax_bits(const uint32_t w[8]) {
   uint32_t m = 0u;
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(w[i] & 0x7FFF7FFFu));
-  const uint32_t lo = m & 0xFFFFu, hi = m >> 16;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(w[i]));
+  const uint32_t lo = m & 0x7FFFu, hi = (m >> 16) & 0x7FFFu;
   // NaN patterns are larger than every finite magnitude and +inf as integers
   return (lo > hi ? lo : hi) << 16;
+}
+
+// Packed fp32 pairs (sm_100 family f32x2 arithmetic): each op rounds both
+// halves exactly as its scalar counterpart (round to nearest, subnormals kept).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
 }
 
 // Correctly rounded x / s from r = RN(1 / s), by P. Markstein's method
@@ -72,12 +96,46 @@ __device__ __forceinline__ float div_rn_markstein(float x, float s, float r) {
   return fmaf(-e, r, q);
 }
 
+// The same two corrections on a pair of quotients x / s.  S2 = {s, s},
+// R2 = {r, r}, NR2 = {-r, -r}: -e * r is formed as e * (-r) (the same
+// product), and -x as x * (-1) + (-0), exact and with the sign of zero
+// flipped as a negation does.
+__device__ __forceinline__ uint64_t div2_rn_markstein(uint64_t x, uint64_t S2, uint64_t R2,
+                                                      uint64_t NR2) {
+  const uint64_t kMinusOne = 0xBF800000BF800000ull, kMinusZero = 0x8000000080000000ull;
+  const uint64_t nx = f2_fma(x, kMinusOne, kMinusZero);
+  uint64_t q = f2_mul(x, R2);
+  uint64_t e = f2_fma(S2, q, nx);
+  q = f2_fma(e, NR2, q);
+  e = f2_fma(S2, q, nx);
+  return f2_fma(e, NR2, q);
+}
+
+// Two bf16 values of a word as a pair of fp32 (low element in the low half).
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Four bytes (the low byte of each word) into one word, c0 lowest.
+__device__ __forceinline__ uint32_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+  return __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
+}
+
+// NVFP4 block-scale table of one tensor: S[c] = RN(dec_E4M3(c) g) for the 128
+// non-negative codes, and RN(1 / S[c]) where the corrected quotient is exact
+// (S in [2^-80, 2^80]), else 0 (those blocks divide in IEEE arithmetic).
+struct NvScaleTable {
+  float S[128];
+  float rS[128];
+};
+
 // Quantizes one 16-element block, already in registers as two 16-byte words of
 // bf16, into row r of the cache: data bytes plus (FP4 formats) one scale byte.
 template <kvq_format F>
 __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t r, int blk, int D, int nb,
                                             const uint4 lo, const uint4 hi, float s, float rs,
-                                            bool fast_div) {
+                                            bool fast_div, const NvScaleTable* tab = nullptr,
+                                            float s6 = 0.f, float rs6 = 0.f) {
   if (F == KVQ_BF16) {
     uint4* d4 = reinterpret_cast<uint4*>(dat + r * (D * 2) + blk * 32);
     d4[0] = lo;
@@ -85,12 +143,6 @@ __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t 
     return;
   }
   const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  float x[16];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
   const uint32_t amax_bits = block_amax_bits(w);
   const bool finite = amax_bits < 0x7F800000u;
 
@@ -98,31 +150,48 @@ __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t 
     // fast path: every quotient finite, residuals exact near the decisions
     const bool fast = fast_div && finite && __uint_as_float(amax_bits) * rs < 1e37f;
     uint32_t wo[4];
+    if (fast) {
+      const uint64_t S2 = f2_pack(s, s), R2 = f2_pack(rs, rs), NR2 = f2_pack(-rs, -rs);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t p[2];
+      for (int i = 0; i < 4; ++i) {
+        uint32_t p[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float x0 = x[4 * i + 2 * j], x1 = x[4 * i + 2 * j + 1];
-        float q0, q1;
-        if (fast) {
-          q0 = div_rn_markstein(x0, s, rs);
-          q1 = div_rn_markstein(x1, s, rs);
-        } else {
-          q0 = x0 / s;  // IEEE fp32 division
-          q1 = x1 / s;
+        for (int j = 0; j < 2; ++j) {
+          float q0, q1;
+          f2_unpack(div2_rn_markstein(bf2_to_f2(w[2 * i + j]), S2, R2, NR2), q0, q1);
+          p[j] = ((F == KVQ_FP8_E4M3) ? enc2_e4m3(q0, q1) : enc2_e5m2(q0, q1)) & 0xFFFFu;
         }
-        uint32_t c = (F == KVQ_FP8_E4M3) ? enc2_e4m3(q0, q1) : enc2_e5m2(q0, q1);
-        if (!finite) {  // NaN input: 0x7F with the input's sign
-          if (x0 != x0) c = (c & 0xFF00u) | 0x7Fu | ((__float_as_uint(x0) >> 24) & 0x80u);
-          if (x1 != x1) c = (c & 0x00FFu) | ((0x7Fu | ((__float_as_uint(x1) >> 24) & 0x80u)) << 8);
-        }
-        p[j] = c & 0xFFFFu;
+        wo[i] = p[0] | (p[1] << 16);
       }
-      wo[i] = p[0] | (p[1] << 16);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t p[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float x0 = __uint_as_float(w[2 * i + j] << 16);
+          const float x1 = __uint_as_float(w[2 * i + j] & 0xFFFF0000u);
+          const float q0 = x0 / s, q1 = x1 / s;  // IEEE fp32 division
+          uint32_t c = (F == KVQ_FP8_E4M3) ? enc2_e4m3(q0, q1) : enc2_e5m2(q0, q1);
+          if (!finite) {  // NaN input: 0x7F with the input's sign
+            if (x0 != x0) c = (c & 0xFF00u) | 0x7Fu | ((__float_as_uint(x0) >> 24) & 0x80u);
+            if (x1 != x1) c = (c & 0x00FFu) | ((0x7Fu | ((__float_as_uint(x1) >> 24) & 0x80u)) << 8);
+          }
+          p[j] = c & 0xFFFFu;
+        }
+        wo[i] = p[0] | (p[1] << 16);
+      }
     }
     *reinterpret_cast<uint4*>(dat + r * D + blk * 16) = make_uint4(wo[0], wo[1], wo[2], wo[3]);
     return;
+  }
+
+  if constexpr (F == KVQ_FP4_BLOCK16 || F == KVQ_NVFP4) {
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
 
   // FP4 formats: block amax, block scale, E2M1 codes.
@@ -136,6 +205,31 @@ __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t 
     if (amax > 0.f) E = max(-127, min(127, floor_log2(amax) - 2));
     scode = (uint32_t)(E + 127);
     mul = exp2i(-E);
+  } else if (tab) {
+    // NVFP4, per-tensor g: sc = E4M3(amax / RN(6 g)) by the corrected
+    // quotient from the precomputed reciprocal; S and 1 / S from the table
+    const bool fr = rs6 != 0.f && finite && amax * rs6 < 1e37f;
+    const float ratio = fr ? div_rn_markstein(amax, s6, rs6) : amax / s6;
+    scode = enc2_e4m3(ratio, 0.f) & 0xFF;
+    S = tab->S[scode & 0x7F];
+    rS = tab->rS[scode & 0x7F];
+    zero = (S == 0.f);
+    fast = finite && !zero && rS != 0.f && amax * rS < 1e37f;
+    if (fast) {  // packed pairs of corrected quotients
+      const uint64_t S2 = f2_pack(S, S), R2 = f2_pack(rS, rS), NR2 = f2_pack(-rS, -rS);
+      uint32_t c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float y0, y1;
+        f2_unpack(div2_rn_markstein(bf2_to_f2(w[i]), S2, R2, NR2), y0, y1);
+        c[i] = enc2_e2m1(y0, y1);
+      }
+      *reinterpret_cast<uint2*>(dat + r * (D / 2) + blk * 8) =
+          make_uint2(pack4(c[0], c[1], c[2], c[3]), pack4(c[4], c[5], c[6], c[7]));
+      scl[r * nb + blk] = (uint8_t)scode;
+      return;
+    }
+    if (!zero) rS = 1.f / S;
   } else {
     // NVFP4: sc = E4M3(amax / (6 g)); S = dec(sc) * g
     const float g = s;
@@ -168,6 +262,7 @@ __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t 
   }
   *reinterpret_cast<uint2*>(dat + r * (D / 2) + blk * 8) = make_uint2(wo[0], wo[1]);
   scl[r * nb + blk] = (uint8_t)scode;
+  }
 }
 
 // Grid-stride loop over items (token, block-of-16) of one of K / V (blockIdx.y),
@@ -179,6 +274,20 @@ __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t 
 template <kvq_format F, bool PH>
 __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
   const int kv = blockIdx.y;
+  // NVFP4 with a per-tensor global scale: the CTA's block-scale table
+  constexpr bool kTable = (F == KVQ_NVFP4) && !PH;
+  const NvScaleTable* tab = nullptr;
+  if constexpr (kTable) {
+    __shared__ NvScaleTable tab_s;
+    const float g = kv ? a.s[1] : a.s[0];
+    if (threadIdx.x < 128) {
+      const float S = __fmul_rn(dec_e4m3(threadIdx.x), g);
+      tab_s.S[threadIdx.x] = S;
+      tab_s.rS[threadIdx.x] = (S >= 0x1p-80f && S <= 0x1p80f) ? 1.0f / S : 0.f;
+    }
+    __syncthreads();
+    tab = &tab_s;
+  }
   // the item index advances by a constant stride, split once into (tokens, blocks)
   const long long S = (long long)gridDim.x * blockDim.x;
   const long long S_tok = S / a.hb;
@@ -233,6 +342,9 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
       if constexpr (PH) {
         const float sh = __ldg(hsp + h), rh = __ldg(hrp + h);
         store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, sh, rh, sh >= 0x1p-80f && sh <= 0x1p80f);
+      } else if constexpr (kTable) {
+        store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, s, rs, a.fast_div, tab,
+                       kv ? a.s6[1] : a.s6[0], kv ? a.rs6[1] : a.rs6[0]);
       } else {
         store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, s, rs, a.fast_div);
       }
@@ -383,6 +495,13 @@ cudaError_t launch_store(const Geometry& g, const LayerView& L, const void* k, c
   a.s[1] = s_v;
   a.rs[0] = 1.0f / s_k;
   a.rs[1] = 1.0f / s_v;
+  // NVFP4 block-scale divisor 6 g and its reciprocal (0: divide in IEEE
+  // arithmetic, outside the range where the corrected quotient is exact)
+  const float gs[2] = {s_k, s_v};
+  for (int i = 0; i < 2; ++i) {
+    a.s6[i] = 6.0f * gs[i];  // one fp32 product, as the quantization rule forms it
+    a.rs6[i] = (a.s6[i] >= 0x1p-80f && a.s6[i] <= 0x1p80f) ? 1.0f / a.s6[i] : 0.f;
+  }
   a.slots = slots;
   a.n = num_tokens;
   a.H = g.kv_heads;

@@ -196,6 +196,41 @@ def test_fp4_block16_wide_exponent_spread(kvq, orc, cuda, spread):
     assert_attention_close(got, ref, f"fp4 block-16 spread 2^{spread}")
 
 
+@pytest.mark.parametrize("pattern", ["early_large", "late_large", "alternating"])
+def test_fp4_block16_token_scale_jumps(kvq, orc, cuda, pattern):
+    """Token groups whose magnitudes jump by 2^6 to 2^12 along the sequence: the
+    K reference exponent is re-anchored per chunk (up and down) and the V
+    running reference is raised mid-segment, while other chunks stay on the
+    packed-integer factor path; long sequences so segments span many chunks."""
+    T = 2000
+    wl = synth.make_workload("jump", "fp4_mx_block16", Hq=16, Hkv=2, seq_lens=[T, 1500], seed=21)
+    t = np.arange(T)
+    if pattern == "early_large":
+        e = np.where(t < 48, 12, 0)
+    elif pattern == "late_large":
+        e = np.where((t > 1200) & (t < 1260), 12, 0) - np.where((t > 400) & (t < 700), 6, 0)
+    else:
+        e = ((t // 64) % 3 - 1) * 6
+    ks, vs = [], []
+    for b in range(wl.B):
+        k, v = wl.kv_float(0, b)
+        # K jumps down where V jumps up: those tokens keep moderate logits, so
+        # every chunk's logits and values carry weight in the output
+        m = torch.from_numpy(2.0 ** e[: k.shape[0]]).float().view(-1, 1, 1)
+        ks.append(synth.to_bf16_bits(k / m))
+        vs.append(synth.to_bf16_bits(v * m))
+    c = gpu_cache_for(kvq, wl)
+    oc = orc.OracleCache(wl.fmt, wl.Hkv, wl.D, wl.P, wl.num_pages)
+    for b in range(wl.B):
+        c.quantize_and_store(0, bits_to_cuda(ks[b]), bits_to_cuda(vs[b]),
+                             torch.from_numpy(wl.slots(b)).cuda(), None)
+        assert oc.quantize_store(ks[b], vs[b], wl.slots(b), None) == 0
+    got = gpu_decode(c, wl)
+    ref, rc = oc.decode_attention(wl.q(), wl.page_table, wl.seq_lens, wl.sm_scale)
+    assert rc == 0 and c.device_error() == 0
+    assert_attention_close(got, ref, f"fp4 block-16 token jumps {pattern}")
+
+
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("L,P", [(34, 16), (48, 16), (49, 16), (100, 32), (200, 64), (47, 48)])
 def test_decode_whole_stages_per_worker(kvq, orc, cuda, fmt, L, P):
