@@ -71,6 +71,12 @@ def _load():
             lib.orc_decode_attention.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp,
                                                  i32, vp, i32, vp, i32, vp, i32, f64, vp]
             lib.orc_decode_attention.restype = i32
+            lib.orc_quantize_query.argtypes = [vp, i64, i32, i32, vp, i32, vp]
+            lib.orc_quantize_query.restype = i32
+            lib.orc_decode_attention_fp8q.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp, vp,
+                                                      vp, vp, i32, i32, vp, i32, vp, i32, vp, i32,
+                                                      f64, vp]
+            lib.orc_decode_attention_fp8q.restype = i32
             lib.orc_calibrate_scales.argtypes = [i32, i32, i32, vp, i32, i32, vp]
             lib.orc_calibrate_scales.restype = i32
             lib.orc_num_threads.argtypes = []
@@ -150,6 +156,18 @@ def calibrate_scales(fmt, x_bf16: np.ndarray, per_head: bool) -> np.ndarray:
     return out
 
 
+def quantize_query(q_bf16: np.ndarray, q_scales) -> np.ndarray:
+    """E4M3 codes of a bf16 query [rows][Hq][D] (reading R17): one q_scale per
+    tensor ([1]) or per q head ([Hq])."""
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    rows, Hq, D = q.shape
+    s = np.ascontiguousarray(np.asarray(q_scales, np.float32).reshape(-1))
+    out = np.zeros((rows, Hq, D), np.uint8)
+    rc = _load().orc_quantize_query(_ptr(q), rows, Hq, D, _ptr(s), s.shape[0], _ptr(out))
+    assert rc == 0, "q_scales must have 1 or Hq entries"
+    return out
+
+
 # --- cache model ------------------------------------------------------------
 
 def data_row_bytes(fmt, head_dim: int) -> int:
@@ -219,6 +237,27 @@ class OracleCache:
                                           _ptr(self.scales), _ptr(q), Hq, _ptr(pt), pt.shape[1],
                                           _ptr(sl), B, _ptr(bl), 0 if bl is None else bl.shape[0],
                                           float(sm_scale), _ptr(out))
+        return out, rc
+
+    def decode_attention_fp8q(self, q_bf16: np.ndarray, q_scales, page_table: np.ndarray,
+                              seq_lens: np.ndarray, sm_scale: float, b_list=None):
+        """Decode attention in the FP8 domain (reading R17): the query is
+        quantized to E4M3 with q_scales ([1] or [Hq]) and attention is exact
+        over the dequantized query.  Returns (out fp64 [B][Hq][D], rc)."""
+        q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+        s = np.ascontiguousarray(np.asarray(q_scales, np.float32).reshape(-1))
+        pt = np.ascontiguousarray(page_table, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, Hq, D = q.shape
+        out = np.zeros((B, Hq, D), np.float64)
+        bl = None if b_list is None else np.ascontiguousarray(b_list, dtype=np.int32)
+        rc = _load().orc_decode_attention_fp8q(self.fmt, self.H, self.D, self.P, self.num_pages,
+                                               _ptr(self.k_data), _ptr(self.v_data),
+                                               _ptr(self.k_scales), _ptr(self.v_scales),
+                                               _ptr(self.scales), _ptr(q), _ptr(s), s.shape[0], Hq,
+                                               _ptr(pt), pt.shape[1], _ptr(sl), B, _ptr(bl),
+                                               0 if bl is None else bl.shape[0], float(sm_scale),
+                                               _ptr(out))
         return out, rc
 
     def extend_attention(self, q_bf16: np.ndarray, q_seq: np.ndarray, q_len: np.ndarray,

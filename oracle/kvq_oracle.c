@@ -51,6 +51,10 @@
  *       with M = 448 (E4M3), 57344 (E5M2), 6 * 448 = 2688 (NVFP4 global scale,
  *       so the largest block scale lands on the E4M3 maximum); amax == 0
  *       gives 1.0, the pages' default scale.
+ *   R17 FP8-domain attention ([VLLM] FP8 KV cache overview; Supported
+ *       schemes): the query is quantized to E4M3 with q_scale (per tensor or
+ *       per q head) by the R2/R3 rule; attention is then exact over the
+ *       dequantized query (the softmax weights are not quantized).
  *   Non-finite K/V values are outside the contract for the FP4 formats.
  *
  * Parity pins: R4 and R5 are this library's own definitions; the pages give
@@ -435,21 +439,22 @@ int orc_dequantize(int fmt, int H, int D, int P, int64_t num_pages, const uint8_
 /* ------------------------------------------------------------------------ */
 
 /*
- * q: bf16 bits [B][Hq][D].  page_table: int32 [B][max_pages]; token t of
- * sequence b lives in page page_table[b][t / P] at offset t % P.
- * For every b in b_list (or every b when b_list is NULL) and every q head j:
- *   z_t = sm_scale * sum_d q[b][j][d] * K^[t][d],  t < seq_lens[b]
+ * Attention core over exact query values qv: fp64 [B][Hq][D].
+ * page_table: int32 [B][max_pages]; token t of sequence b lives in page
+ * page_table[b][t / P] at offset t % P.  For every b in b_list (or every b
+ * when b_list is NULL) and every q head j:
+ *   z_t = sm_scale * sum_d qv[b][j][d] * K^[t][d],  t < seq_lens[b]
  *   out[b][j][:] = sum_t softmax(z)_t * V^[t][:]
  * with K^, V^ the exact dequantized values (scales [2][H] as for the store).
- * Output rows of sequences not in
- * b_list are left untouched.  Returns 0, or -1 if a page id is out of range
- * (the affected rows are set to zero).
+ * Output rows of sequences not in b_list are left untouched.  Returns 0, or
+ * -1 if a page id or length is out of range (the affected rows are set to
+ * zero).
  */
-int orc_decode_attention(int fmt, int H, int D, int P, int64_t num_pages, const uint8_t* k_data,
-                         const uint8_t* v_data, const uint8_t* k_scl, const uint8_t* v_scl,
-                         const float* scales, const uint16_t* q, int Hq,
-                         const int32_t* page_table, int max_pages, const int32_t* seq_lens,
-                         int B, const int32_t* b_list, int nb, double sm_scale, double* out) {
+static int attention_core(int fmt, int H, int D, int P, int64_t num_pages, const uint8_t* k_data,
+                          const uint8_t* v_data, const uint8_t* k_scl, const uint8_t* v_scl,
+                          const float* scales, const double* qv, int Hq,
+                          const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                          int B, const int32_t* b_list, int nb, double sm_scale, double* out) {
   int G, bad = 0;
   int nsel = b_list ? nb : B;
   size_t drow = data_row_bytes(fmt, D), srow = (size_t)D / 16;
@@ -465,16 +470,13 @@ int orc_decode_attention(int fmt, int H, int D, int P, int64_t num_pages, const 
     int T = seq_lens[b];
     double* z = NULL;
     double* kv = (double*)malloc(sizeof(double) * (size_t)D);
-    double* qd = (double*)malloc(sizeof(double) * (size_t)G * D);
     double* acc = (double*)calloc((size_t)G * D, sizeof(double));
     double* m = (double*)malloc(sizeof(double) * (size_t)G);
     double* l = (double*)calloc((size_t)G, sizeof(double));
+    const double* qd = qv + ((size_t)b * Hq + (size_t)h * G) * D;   /* the group's G heads */
     int ok = 1;
     if (T < 0 || T > max_pages * P) ok = 0;
     if (ok && T > 0) z = (double*)malloc(sizeof(double) * (size_t)G * T);
-    for (int g = 0; g < G; ++g)
-      for (int d = 0; d < D; ++d)
-        qd[g * D + d] = orc_dec_bf16(q[((size_t)b * Hq + (size_t)h * G + g) * D + d]);
     /* pass 1: logits */
     for (int t = 0; ok && t < T; ++t) {
       int32_t page = page_table[(size_t)b * max_pages + t / P];
@@ -515,9 +517,80 @@ int orc_decode_attention(int fmt, int H, int D, int P, int64_t num_pages, const 
       for (int d = 0; d < D; ++d) o[d] = (ok && T > 0) ? acc[g * D + d] / l[g] : 0.0;
     }
     if (!ok) bad = 1;
-    free(z); free(kv); free(qd); free(acc); free(m); free(l);
+    free(z); free(kv); free(acc); free(m); free(l);
   }
   return bad ? -1 : 0;
+}
+
+/* Decode attention of a bf16 query q: bits [B][Hq][D] (R9); see attention_core. */
+int orc_decode_attention(int fmt, int H, int D, int P, int64_t num_pages, const uint8_t* k_data,
+                         const uint8_t* v_data, const uint8_t* k_scl, const uint8_t* v_scl,
+                         const float* scales, const uint16_t* q, int Hq,
+                         const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                         int B, const int32_t* b_list, int nb, double sm_scale, double* out) {
+  size_t n = (size_t)B * Hq * D;
+  double* qv = (double*)malloc(sizeof(double) * (n ? n : 1));
+  int rc;
+  for (size_t i = 0; i < n; ++i) qv[i] = orc_dec_bf16(q[i]);
+  rc = attention_core(fmt, H, D, P, num_pages, k_data, v_data, k_scl, v_scl, scales, qv, Hq,
+                      page_table, max_pages, seq_lens, B, b_list, nb, sm_scale, out);
+  free(qv);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention in the FP8 domain with a quantized query (R17)                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [VLLM] FP8 KV cache overview: with an FP8 cache on the Flash Attention 3
+ * backend the attention itself runs in the quantized (FP8) domain and the
+ * query is quantized to FP8 as well; Supported schemes: q_scale is one value
+ * per tensor ([1]) or one per attention head ([num_heads]).
+ * R17: the query is quantized like the cache's FP8 E4M3 store (R2, R3):
+ *   code = enc_E4M3(q / q_scale) (fp32 division, nearest, ties to even,
+ *   saturating; NaN gives 0x7F with its sign), q_scale = q_scales[0] for
+ *   nq == 1, else q_scales[j] for q head j.
+ * q: bf16 bits [rows][Hq][D]; codes: [rows][Hq][D] bytes.
+ */
+int orc_quantize_query(const uint16_t* q, int64_t rows, int Hq, int D, const float* q_scales,
+                       int nq, uint8_t* codes) {
+  if (nq != 1 && nq != Hq) return -2;
+  for (int64_t i = 0; i < rows * Hq; ++i) {
+    const float s = q_scales[nq == 1 ? 0 : (int)(i % Hq)];
+    for (int d = 0; d < D; ++d) {
+      float x = bf16_to_float(q[i * D + d]);
+      float y = x / s;                                         /* R3: fp32 division */
+      codes[i * D + d] = isnan(x) ? (uint8_t)(0x7Fu | (signbit(x) ? 0x80u : 0u))
+                                  : (uint8_t)orc_enc_e4m3(y);
+    }
+  }
+  return 0;
+}
+
+/* Decode attention with the query quantized by orc_quantize_query: the same
+ * attention over the exact query values dec_E4M3(code) * q_scale (fp64). */
+int orc_decode_attention_fp8q(int fmt, int H, int D, int P, int64_t num_pages,
+                              const uint8_t* k_data, const uint8_t* v_data, const uint8_t* k_scl,
+                              const uint8_t* v_scl, const float* scales, const uint16_t* q,
+                              const float* q_scales, int nq, int Hq, const int32_t* page_table,
+                              int max_pages, const int32_t* seq_lens, int B, const int32_t* b_list,
+                              int nb, double sm_scale, double* out) {
+  size_t n = (size_t)B * Hq * D;
+  uint8_t* codes = (uint8_t*)malloc(n ? n : 1);
+  double* qv = (double*)malloc(sizeof(double) * (n ? n : 1));
+  int rc = orc_quantize_query(q, B, Hq, D, q_scales, nq, codes);
+  if (rc == 0) {
+    for (size_t i = 0; i < n; ++i) {
+      const size_t j = (i / (size_t)D) % (size_t)Hq;
+      qv[i] = orc_dec_e4m3(codes[i]) * (double)q_scales[nq == 1 ? 0 : j];
+    }
+    rc = attention_core(fmt, H, D, P, num_pages, k_data, v_data, k_scl, v_scl, scales, qv, Hq,
+                        page_table, max_pages, seq_lens, B, b_list, nb, sm_scale, out);
+  }
+  free(codes);
+  free(qv);
+  return rc;
 }
 
 /* Threads the OpenMP runtime will use (reported beside timings). */
