@@ -370,6 +370,20 @@ def per_format_cells(args, wl, ks, vs, d_q, d_pt, d_sl, exact, dev, peak):
                     "bytes_per_call": nbytes, "calls": steps,
                     "quant_error": {k: (round(v, 6) if isinstance(v, float) else v)
                                     for k, v in quant_error(out_rows(out, exact.keys()), exact).items()}}
+        if f in ("fp8_e4m3", "fp8_e5m2"):
+            # FP8-domain attention: the query quantized to E4M3 (per-tensor
+            # q_scale = amax / 448), QK^T on FP8 tensor cores
+            qs = [float(x) for x in wl.q_scales(0)]
+            ms = _time_calls(lambda: cache.decode_attention_fp8q(0, d_q, qs, d_pt, d_sl, wl.sm_scale,
+                                                                 out, ws), steps, warm)
+            if cache.device_error() != 0:
+                raise RuntimeError(f"device error in the {f} FP8-query decode")
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            cells[f + "+fp8_query"] = {
+                "ms_per_call": round(ms, 5), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                "bytes_per_call": nbytes, "calls": steps, "q_scale": qs[0],
+                "quant_error": {k: (round(v, 6) if isinstance(v, float) else v)
+                                for k, v in quant_error(out_rows(out, exact.keys()), exact).items()}}
         cache.close()
     del kall, vall
     return cells

@@ -221,6 +221,46 @@ kvq_status kvq_extend_attention(kvq_cache* cache, int layer, const void* q_bf16,
                                 float sm_scale, void* out_bf16, void* workspace,
                                 size_t workspace_bytes, kvq_stream stream);
 
+/*
+ * Decode attention in the FP8 domain with a quantized query ([VLLM] FP8 KV
+ * cache overview: with an FP8 KV cache on the Flash Attention 3 backend the
+ * attention itself is computed in the quantized (FP8) domain and the query is
+ * quantized to FP8 together with keys and values; [VLLM] Supported schemes:
+ * q_scale is [1] per tensor or [num_heads] per attention head).
+ *   q_scales (host): num_q_scales = 1 (per tensor) or num_q_heads floats
+ *                    (per q head), finite and > 0, at most 256.
+ * Every q head j is quantized to E4M3 with the store's rule: code =
+ * enc_E4M3(q / q_scale_j) (fp32 division, nearest, ties to even, saturating),
+ * and QK^T runs on FP8 tensor cores over the query codes and the cache's FP8
+ * codes unconverted; the softmax weights and the PV product keep f16/fp32
+ * precision (they are not quantized).  The result is attention over the
+ * dequantized query q^ = dec(code) * q_scale_j:
+ *   out[b][j] = sum_t softmax_t(sm_scale * q^[b][j] . K^[t]) V^[t].
+ * Only for fp8_e4m3 and fp8_e5m2 caches (others: KVQ_ERR_UNSUPPORTED).  All
+ * other arguments, the workspace (same size as kvq_decode_attention's), the
+ * rules and the errors are those of kvq_decode_attention.
+ */
+kvq_status kvq_decode_attention_fp8q(kvq_cache* cache, int layer, const void* q_bf16,
+                                     int num_q_heads, const float* q_scales, int num_q_scales,
+                                     const int32_t* page_table, int max_pages_per_seq,
+                                     const int32_t* seq_lens, int batch, float sm_scale,
+                                     void* out_bf16, void* workspace, size_t workspace_bytes,
+                                     kvq_stream stream);
+
+/*
+ * The query quantization of kvq_decode_attention_fp8q on its own ([VLLM] FP8
+ * KV cache overview; Supported schemes), for callers that keep the FP8 query:
+ *   q_bf16:   [rows][num_q_heads][head_dim] bf16 device rows, 16-byte aligned.
+ *   q_scales: host, 1 or num_q_heads floats (finite, > 0, at most 256).
+ *   q_codes:  [rows][num_q_heads][head_dim] E4M3 bytes (device, 16-byte
+ *             aligned): enc_E4M3(q / q_scale) per element, NaN -> 0x7F with
+ *             its sign.
+ * head_dim % 16 == 0.  No cache needed.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+kvq_status kvq_quantize_query(const void* q_bf16, int rows, int num_q_heads, int head_dim,
+                              const float* q_scales, int num_q_scales, void* q_codes,
+                              kvq_stream stream);
+
 /* Bytes of workspace kvq_decode_attention needs for these sizes (0 on invalid
  * arguments; see kvq_last_error_string). */
 size_t kvq_decode_workspace_size(const kvq_cache* cache, int batch, int num_q_heads,

@@ -35,6 +35,9 @@ def _load():
         "kvq_layer_head_scales": ([vp, i32, ctypes.POINTER(f32), ctypes.POINTER(f32), vp], i32),
         "kvq_decode_attention": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp, sz, vp], i32),
         "kvq_decode_workspace_size": ([vp, i32, i32, i32], sz),
+        "kvq_decode_attention_fp8q": ([vp, i32, vp, i32, ctypes.POINTER(f32), i32, vp, i32, vp, i32,
+                                       f32, vp, vp, sz, vp], i32),
+        "kvq_quantize_query": ([vp, i32, i32, i32, ctypes.POINTER(f32), i32, vp, vp], i32),
         "kvq_extend_attention": ([vp, i32, vp, i32, i32, vp, vp, vp, i32, i32, f32, vp, vp, sz, vp],
                                  i32),
         "kvq_decode_attention_noalloc": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp], i32),
@@ -168,6 +171,32 @@ def kvq_decode_attention(handle, layer, q, page_table, seq_lens, sm_scale, out, 
            "kvq_decode_attention")
 
 
+def _floats(x):
+    x = [float(t) for t in x]
+    return (ctypes.c_float * len(x))(*x), len(x)
+
+
+def kvq_decode_attention_fp8q(handle, layer, q, q_scales, page_table, seq_lens, sm_scale, out,
+                              workspace, stream=None):
+    """FP8-domain decode attention: q bf16 [B][Hq][D] quantized to E4M3 with
+    q_scales (host sequence of 1 or Hq floats); otherwise as kvq_decode_attention."""
+    B, Hq, _ = q.shape
+    qs, nqs = _floats(q_scales)
+    _check(lib.kvq_decode_attention_fp8q(ctypes.c_void_p(handle), layer, _ptr(q), Hq, qs, nqs,
+                                         _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens),
+                                         B, float(sm_scale), _ptr(out), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream(stream)), "kvq_decode_attention_fp8q")
+
+
+def kvq_quantize_query(q, q_scales, codes, stream=None):
+    """E4M3 codes (uint8 device tensor, q's shape) of a bf16 query [rows][Hq][D]."""
+    rows, Hq, D = q.shape
+    qs, nqs = _floats(q_scales)
+    _check(lib.kvq_quantize_query(_ptr(q), rows, Hq, D, qs, nqs, _ptr(codes), _stream(stream)),
+           "kvq_quantize_query")
+
+
 def kvq_extend_attention(handle, layer, q, q_seq, q_len, page_table, sm_scale, out, workspace,
                          stream=None):
     """q, out: bf16 [n][Hq][D]; q_seq, q_len: int32 [n]; page_table int32 [S][max_pages]."""
@@ -263,6 +292,18 @@ class KVQCache:
             workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
         kvq_decode_attention(self.handle, layer, q, page_table, seq_lens, sm_scale, out, workspace,
                              stream)
+        return out
+
+    def decode_attention_fp8q(self, layer, q, q_scales, page_table, seq_lens, sm_scale, out=None,
+                              workspace=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        if workspace is None:
+            n = self.workspace_size(q.shape[0], q.shape[1], page_table.shape[1])
+            workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+        kvq_decode_attention_fp8q(self.handle, layer, q, q_scales, page_table, seq_lens, sm_scale,
+                                  out, workspace, stream)
         return out
 
     def extend_attention(self, layer, q, q_seq, q_len, page_table, sm_scale, out=None,

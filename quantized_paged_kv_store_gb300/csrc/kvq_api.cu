@@ -130,6 +130,18 @@ kvq_status check_scale_values(const float* s, int n) {
   return KVQ_OK;
 }
 
+// FP8-domain attention query scales: host array of 1 (per tensor) or
+// num_q_heads (per head) finite positive values, at most kMaxQScales.
+kvq_status check_query_scales(const float* q_scales, int n, int num_q_heads) {
+  if (!q_scales) return fail(KVQ_ERR_INVALID_ARG, "q_scales is NULL");
+  if (n != 1 && n != num_q_heads)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_scales must be 1 or num_q_heads (%d); got %d",
+                num_q_heads, n);
+  if (n > kvq::kMaxQScales)
+    return fail(KVQ_ERR_UNSUPPORTED, "at most %d per-head query scales", kvq::kMaxQScales);
+  return check_scale_values(q_scales, n);
+}
+
 kvq_status check_rows(const kvq_cache* c, const void* k, const void* v) {
   if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
   if (!aligned16(k) || !aligned16(v)) return fail(KVQ_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
@@ -508,6 +520,57 @@ kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q_bf16, int
                                      head_scales(c, layer), nullptr, 0, out_bf16, workspace, c->err,
                                      (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention_fp8q(kvq_cache* c, int layer, const void* q_bf16, int num_q_heads,
+                                     const float* q_scales, int num_q_scales,
+                                     const int32_t* page_table, int max_pages_per_seq,
+                                     const int32_t* seq_lens, int batch, float sm_scale,
+                                     void* out_bf16, void* workspace, size_t workspace_bytes,
+                                     kvq_stream stream) {
+  kvq_status st = check_layer(c, layer);
+  if (st) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0)
+    return fail(KVQ_ERR_INVALID_ARG, "invalid batch / num_q_heads / max_pages_per_seq");
+  if (!std::isfinite(sm_scale)) return fail(KVQ_ERR_INVALID_ARG, "sm_scale must be finite");
+  if ((st = check_query_scales(q_scales, num_q_scales, num_q_heads))) return st;
+  kvq::DecodePlan plan;
+  const char* why = nullptr;
+  if (!kvq::plan_decode(c->geo, batch, num_q_heads, max_pages_per_seq, c->device, &plan, &why, true))
+    return fail(KVQ_ERR_UNSUPPORTED, "%s", why);
+  if (batch == 0) return KVQ_OK;
+  if (!q_bf16 || !page_table || !seq_lens || !out_bf16 || !workspace)
+    return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+  if (!aligned16(q_bf16) || !aligned16(out_bf16) || !aligned16(workspace))
+    return fail(KVQ_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
+  if (workspace_bytes < plan.ws_bytes)
+    return fail(KVQ_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, plan.ws_bytes);
+  if ((st = check_device(c))) return st;
+  float kf, vf;
+  tensor_scales(c, layer, &kf, &vf);
+  cudaError_t e = kvq::launch_decode(c->geo, view(c, layer), plan, q_bf16, num_q_heads, page_table,
+                                     max_pages_per_seq, seq_lens, batch, sm_scale, kf, vf,
+                                     head_scales(c, layer), nullptr, 0, out_bf16, workspace, c->err,
+                                     (cudaStream_t)stream, q_scales, num_q_scales);
+  if (e != cudaSuccess) return cuda_fail(e, "FP8-domain decode attention launch");
+  return KVQ_OK;
+}
+
+kvq_status kvq_quantize_query(const void* q_bf16, int rows, int num_q_heads, int head_dim,
+                              const float* q_scales, int num_q_scales, void* q_codes,
+                              kvq_stream stream) {
+  if (rows < 0 || num_q_heads <= 0 || head_dim <= 0 || head_dim % 16)
+    return fail(KVQ_ERR_INVALID_ARG, "invalid rows / num_q_heads / head_dim (a multiple of 16)");
+  kvq_status st = check_query_scales(q_scales, num_q_scales, num_q_heads);
+  if (st) return st;
+  if (rows == 0) return KVQ_OK;
+  if (!q_bf16 || !q_codes) return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
+  if (!aligned16(q_bf16) || !aligned16(q_codes))
+    return fail(KVQ_ERR_INVALID_ARG, "q and q_codes must be 16-byte aligned");
+  cudaError_t e = kvq::launch_quantize_query(q_bf16, rows, num_q_heads, head_dim, q_scales,
+                                             num_q_scales, q_codes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "query quantization launch");
   return KVQ_OK;
 }
 

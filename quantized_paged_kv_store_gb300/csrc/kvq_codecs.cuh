@@ -113,4 +113,83 @@ __device__ __forceinline__ uint32_t bf16_rne_bits(float x) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
+// Packed fp32 pairs (sm_100 family f32x2 arithmetic): each op rounds both
+// halves exactly as its scalar counterpart (round to nearest, subnormals kept).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Correctly rounded x / s from r = RN(1 / s), by P. Markstein's method
+// ("Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): q = RN(x r) is within 1.5 ulp;
+// one correction q + r (x - s q) (residual exact with a fused multiply-add)
+// makes it faithful, and by Markstein's theorem a second correction from a
+// faithful quotient yields RN(x / s).  Requires a finite quotient (the callers
+// bound the block maximum times r).  The residual is exact unless it underflows,
+// which with s in [2^-89, 2^80] happens only for quotients below 2^-14; there the
+// correction is off by less than 2^-60, far from every rounding decision of the
+// target codes (the smallest, 2^-17, is E5M2's half subnormal).  The residual is
+// formed as s q - x so that signed zeros keep their sign.
+__device__ __forceinline__ float div_rn_markstein(float x, float s, float r) {
+  float q = x * r;
+  float e = fmaf(s, q, -x);
+  q = fmaf(-e, r, q);
+  e = fmaf(s, q, -x);
+  return fmaf(-e, r, q);
+}
+
+// The same two corrections on a pair of quotients x / s.  S2 = {s, s},
+// R2 = {r, r}, NR2 = {-r, -r}: -e * r is formed as e * (-r) (the same
+// product), and -x as x * (-1) + (-0), exact and with the sign of zero
+// flipped as a negation does.
+__device__ __forceinline__ uint64_t div2_rn_markstein(uint64_t x, uint64_t S2, uint64_t R2,
+                                                      uint64_t NR2) {
+  const uint64_t kMinusOne = 0xBF800000BF800000ull, kMinusZero = 0x8000000080000000ull;
+  const uint64_t nx = f2_fma(x, kMinusOne, kMinusZero);
+  uint64_t q = f2_mul(x, R2);
+  uint64_t e = f2_fma(S2, q, nx);
+  q = f2_fma(e, NR2, q);
+  e = f2_fma(S2, q, nx);
+  return f2_fma(e, NR2, q);
+}
+
+// Two bf16 values of a word as a pair of fp32 (low element in the low half).
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// E4M3 codes of x0 / s and x1 / s (low byte from x0): the quotient is the
+// correctly rounded fp32 division (corrected from rs = RN(1 / s) when `fast`,
+// i.e. s in [2^-80, 2^80] and both quotients finite, else IEEE division),
+// encoded to nearest, ties to even, saturating; NaN gives 0x7F with its sign.
+__device__ __forceinline__ uint32_t quant2_e4m3(float x0, float x1, float s, float rs, bool fast) {
+  float q0, q1;
+  if (fast) {
+    f2_unpack(div2_rn_markstein(f2_pack(x0, x1), f2_pack(s, s), f2_pack(rs, rs), f2_pack(-rs, -rs)),
+              q0, q1);
+  } else {
+    q0 = x0 / s;
+    q1 = x1 / s;
+  }
+  uint32_t c = enc2_e4m3(q0, q1);
+  if (x0 != x0) c = (c & 0xFF00u) | 0x7Fu | ((__float_as_uint(x0) >> 24) & 0x80u);
+  if (x1 != x1) c = (c & 0x00FFu) | ((0x7Fu | ((__float_as_uint(x1) >> 24) & 0x80u)) << 8);
+  return c & 0xFFFFu;
+}
+
 }  // namespace kvq

@@ -116,6 +116,22 @@ __device__ __forceinline__ void mma_bf16(float d[4], uint32_t a0, uint32_t a1, u
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// FP8 tensor-core MMA (m16n8k32): A = K codes (E4M3 or E5M2), B = E4M3 query
+// codes, fp32 accumulate.
+template <kvq_format F>
+__device__ __forceinline__ void mma_f8(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                       uint32_t b0, uint32_t b1) {
+  if (F == KVQ_FP8_E5M2)
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e5m2.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t r;
   asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
@@ -184,12 +200,28 @@ struct Ring {
 // 2q+1 (before the per-head scale).  FP4 block-16: kf holds the half2 block
 // factors 2^(E - kref) of (row r, block 2q), (r, 2q+1), (r+8, 2q), (r+8, 2q+1),
 // each broadcast to both halves; 2^kref is applied with the per-head scale.
-template <kvq_format F>
+// QF8 (FP8-domain attention, FP8 caches): qb[j] holds the E4M3 query codes of
+// k-step j of m16n8k32 (k = 4q + i <-> d = 32q + 8j + i, k = 16 + 4q + i <->
+// d = 32q + 8j + 4 + i), and the K codes enter the MMA unconverted.
+template <kvq_format F, bool QF8>
 __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, int r, int q,
                                         const uint32_t (&qb)[8][2], float (&s)[4],
                                         const uint32_t (&kf)[4]) {
   s[0] = s[1] = s[2] = s[3] = 0.f;
-  if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
+  if constexpr (QF8) {
+    const uint4 x0 = lds128(sK + r * 128 + q * 32), x1 = lds128(sK + r * 128 + q * 32 + 16);
+    const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
+    const uint32_t kr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const uint32_t kr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+    float s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      mma_f8<F>((j & 1) ? s2 : s, kr[2 * j], kr8[2 * j], kr[2 * j + 1], kr8[2 * j + 1], qb[j][0], qb[j][1]);
+    s[0] += s2[0];
+    s[1] += s2[1];
+    s[2] += s2[2];
+    s[3] += s2[3];
+  } else if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
     const uint4 x0 = lds128(sK + r * 128 + q * 32), x1 = lds128(sK + r * 128 + q * 32 + 16);
     const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
     const uint32_t kr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -438,7 +470,7 @@ __device__ __forceinline__ void tile_pv(const uint8_t* sV, const uint8_t* sVs, i
 }
 
 // One worker's contribution to unit (b, h, hg) over tiles [t0, t1).
-template <kvq_format F>
+template <kvq_format F, bool QF8>
 __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, int hg, int t0, int t1) {
   using Tr = Traits<F>;
   constexpr int S = Tr::kStages, TPS = Tr::kTps;
@@ -469,7 +501,33 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
 #pragma unroll
       for (int i = 0; i < 16; ++i) w16[i] = 0u;
     }
-    if (F == KVQ_BF16) {
+    if constexpr (QF8) {
+      // FP8-domain attention: E4M3 codes of q / q_scale (the query quantization
+      // rule of the store), the B operand of the m16n8k32 FP8 MMAs
+      const int head = h * a.G + hg * kGroupMax + r;
+      const float qsc = a.qsc[(a.nqs == 1 || r >= gh) ? 0 : head];
+      const float rq = 1.0f / qsc;
+      uint32_t m2 = 0u;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(w16[i]));
+      const float amax = __uint_as_float(max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu) << 16);
+      const bool fast = qsc >= 0x1p-80f && qsc <= 0x1p80f && amax * rq < 1e37f;  // NaN: false
+      uint32_t c[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        c[i] = quant2_e4m3(bf16_bits_to_float(w16[i] & 0xFFFF), bf16_bits_to_float(w16[i] >> 16),
+                           qsc, rq, fast);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        qb[j][0] = c[4 * j] | (c[4 * j + 1] << 16);
+        qb[j][1] = c[4 * j + 2] | (c[4 * j + 3] << 16);
+      }
+#pragma unroll
+      for (int j = 4; j < 8; ++j) qb[j][0] = qb[j][1] = 0u;
+      const float qs = a.kfac ? a.qscale * __ldg(a.kfac + h) : a.qscale;
+      colscale = (r < gh) ? qs * qsc : 1.f;
+    } else if (F == KVQ_BF16) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         qb[j][0] = w16[2 * j];
@@ -681,7 +739,7 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
           kf[2] = __byte_perm(h1, 0, 0x1010);
           kf[3] = __byte_perm(h1, 0, 0x3232);
         }
-        tile_qk<F>(tb, tb + 2 * Tr::kData, r, q, qb, sc[tt], kf);
+        tile_qk<F, QF8>(tb, tb + 2 * Tr::kData, r, q, qb, sc[tt], kf);
         if (!FULL && nvalid[tt] < kTile) {
           if (r >= nvalid[tt]) sc[tt][0] = sc[tt][1] = -INFINITY;
           if (r + 8 >= nvalid[tt]) sc[tt][2] = sc[tt][3] = -INFINITY;
@@ -785,7 +843,7 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
   }
 }
 
-template <kvq_format F>
+template <kvq_format F, bool QF8>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs a) {
   using Tr = Traits<F>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -876,7 +934,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 4) decode_kernel(DecodeArgs
   long long pos = start;
   while (pos < end) {
     const int n = (int)min((long long)(nt - tile), end - pos);
-    segment<F>(a, ring, w, b, ub / a.HG, ub % a.HG, tile, tile + n);
+    segment<F, QF8>(a, ring, w, b, ub / a.HG, ub % a.HG, tile, tile + n);
     pos += n;
     tile += n;
     if (tile == nt) {
@@ -906,7 +964,7 @@ constexpr int kMaxDevices = 64;
 // Kernel attributes are per device: the dynamic shared-memory opt-in and the
 // occupancy query run once for each (format, device), with that device
 // current, under a lock; later calls read the cached CTA count.
-template <kvq_format F>
+template <kvq_format F, bool QF8>
 cudaError_t prepare(int device, int* ctas_per_sm) {
   static std::mutex mu;
   static std::atomic<int> cached[kMaxDevices];
@@ -920,11 +978,11 @@ cudaError_t prepare(int device, int* ctas_per_sm) {
       cudaError_t e = cudaGetDevice(&prev);
       if (e != cudaSuccess) return e;
       if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(decode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(decode_kernel<F, QF8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                Traits<F>::kCtaSmem);
       int occ = 0;
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<F>, kWarpsPerCta * 32,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<F, QF8>, kWarpsPerCta * 32,
                                                           Traits<F>::kCtaSmem);
       if (prev != device) {
         const cudaError_t e2 = cudaSetDevice(prev);
@@ -939,27 +997,34 @@ cudaError_t prepare(int device, int* ctas_per_sm) {
   return cudaSuccess;
 }
 
-cudaError_t ctas_per_sm(kvq_format f, int device, int* n) {
+cudaError_t ctas_per_sm(kvq_format f, bool qf8, int device, int* n) {
+  if (qf8) {
+    switch (f) {
+      case KVQ_FP8_E4M3: return prepare<KVQ_FP8_E4M3, true>(device, n);
+      case KVQ_FP8_E5M2: return prepare<KVQ_FP8_E5M2, true>(device, n);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (f) {
-    case KVQ_BF16: return prepare<KVQ_BF16>(device, n);
-    case KVQ_FP8_E4M3: return prepare<KVQ_FP8_E4M3>(device, n);
-    case KVQ_FP8_E5M2: return prepare<KVQ_FP8_E5M2>(device, n);
-    case KVQ_FP4_BLOCK16: return prepare<KVQ_FP4_BLOCK16>(device, n);
-    case KVQ_NVFP4: return prepare<KVQ_NVFP4>(device, n);
+    case KVQ_BF16: return prepare<KVQ_BF16, false>(device, n);
+    case KVQ_FP8_E4M3: return prepare<KVQ_FP8_E4M3, false>(device, n);
+    case KVQ_FP8_E5M2: return prepare<KVQ_FP8_E5M2, false>(device, n);
+    case KVQ_FP4_BLOCK16: return prepare<KVQ_FP4_BLOCK16, false>(device, n);
+    case KVQ_NVFP4: return prepare<KVQ_NVFP4, false>(device, n);
   }
   return cudaErrorInvalidValue;
 }
 
-template <kvq_format F>
+template <kvq_format F, bool QF8>
 cudaError_t launch_f(const DecodeArgs& a, int ctas, cudaStream_t stream) {
-  decode_kernel<F><<<ctas, kWarpsPerCta * 32, Traits<F>::kCtaSmem, stream>>>(a);
+  decode_kernel<F, QF8><<<ctas, kWarpsPerCta * 32, Traits<F>::kCtaSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_per_seq,
-                 int device, DecodePlan* plan, const char** why) {
+                 int device, DecodePlan* plan, const char** why, bool qf8) {
   if (g.head_dim != kHeadDim) { *why = "decode attention supports head_dim == 128 only"; return false; }
   if (g.page_size % kTile != 0) { *why = "decode attention needs page_size % 16 == 0"; return false; }
   if (num_q_heads % g.kv_heads != 0) { *why = "num_q_heads must be a multiple of kv_heads"; return false; }
@@ -974,9 +1039,22 @@ bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_pe
     *why = "cannot query the SM count";
     return false;
   }
-  if (ctas_per_sm(g.fmt, device, &per_sm) != cudaSuccess) {
+  // the grid (and so the workspace) is sized from the bf16-query kernel of the
+  // format; the FP8-query kernel has the same shared memory and register bound
+  if (ctas_per_sm(g.fmt, false, device, &per_sm) != cudaSuccess) {
     *why = "cannot configure the decode kernel";
     return false;
+  }
+  if (qf8) {
+    int per_sm_q = 0;
+    if (g.fmt != KVQ_FP8_E4M3 && g.fmt != KVQ_FP8_E5M2) {
+      *why = "FP8-domain attention needs an fp8_e4m3 or fp8_e5m2 cache";
+      return false;
+    }
+    if (ctas_per_sm(g.fmt, true, device, &per_sm_q) != cudaSuccess) {
+      *why = "cannot configure the FP8-domain decode kernel";
+      return false;
+    }
   }
   plan->group = G;
   plan->head_groups = (G + kGroupMax - 1) / kGroupMax;
@@ -1001,8 +1079,11 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
                           int max_pages_per_seq, const int32_t* seq_lens, int batch,
                           float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
                           const int32_t* pt_rows, int pt_nrows, void* out, void* workspace,
-                          int* err, cudaStream_t stream) {
+                          int* err, cudaStream_t stream, const float* q_scales, int num_q_scales) {
   DecodeArgs a;
+  const bool qf8 = q_scales != nullptr;
+  a.nqs = qf8 ? num_q_scales : 0;
+  for (int i = 0; i < kMaxQScales; ++i) a.qsc[i] = (qf8 && i < num_q_scales) ? q_scales[i] : 1.0f;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.part_o = reinterpret_cast<float*>(ws);
   ws += align256((size_t)plan.num_slots * kGroupMax * kHeadDim * sizeof(float));
@@ -1042,12 +1123,20 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
   a.fault_wait = fault && std::strcmp(fault, "wait") == 0;
   if (batch == 0) return cudaSuccess;
   cudaError_t e = cudaErrorInvalidValue;
-  switch (g.fmt) {
-    case KVQ_BF16: e = launch_f<KVQ_BF16>(a, plan.ctas, stream); break;
-    case KVQ_FP8_E4M3: e = launch_f<KVQ_FP8_E4M3>(a, plan.ctas, stream); break;
-    case KVQ_FP8_E5M2: e = launch_f<KVQ_FP8_E5M2>(a, plan.ctas, stream); break;
-    case KVQ_FP4_BLOCK16: e = launch_f<KVQ_FP4_BLOCK16>(a, plan.ctas, stream); break;
-    case KVQ_NVFP4: e = launch_f<KVQ_NVFP4>(a, plan.ctas, stream); break;
+  if (qf8) {
+    switch (g.fmt) {
+      case KVQ_FP8_E4M3: e = launch_f<KVQ_FP8_E4M3, true>(a, plan.ctas, stream); break;
+      case KVQ_FP8_E5M2: e = launch_f<KVQ_FP8_E5M2, true>(a, plan.ctas, stream); break;
+      default: break;
+    }
+  } else {
+    switch (g.fmt) {
+      case KVQ_BF16: e = launch_f<KVQ_BF16, false>(a, plan.ctas, stream); break;
+      case KVQ_FP8_E4M3: e = launch_f<KVQ_FP8_E4M3, false>(a, plan.ctas, stream); break;
+      case KVQ_FP8_E5M2: e = launch_f<KVQ_FP8_E5M2, false>(a, plan.ctas, stream); break;
+      case KVQ_FP4_BLOCK16: e = launch_f<KVQ_FP4_BLOCK16, false>(a, plan.ctas, stream); break;
+      case KVQ_NVFP4: e = launch_f<KVQ_NVFP4, false>(a, plan.ctas, stream); break;
+    }
   }
   if (e != cudaSuccess) return e;
   return launch_merge(a, plan.num_units, stream);

@@ -9,6 +9,7 @@ namespace kvq {
 constexpr int kHeadDim = 128;
 constexpr int kTile = 16;     // tokens per tile
 constexpr int kGroupMax = 8;  // q heads per unit
+constexpr int kMaxQScales = 256;  // FP8-domain attention: q scales carried in the launch
 
 struct DecodeArgs {
   const uint16_t* q;
@@ -34,6 +35,8 @@ struct DecodeArgs {
   const int32_t* pt_rows;  // extend: page-table row of each query token b (or null: row b)
   int pt_nrows;            // rows of the page table when pt_rows is set
   int fault_wait;          // failure-detection test: each warp's first stage wait runs out
+  int nqs;                 // FP8-domain attention: 1 (per tensor) or Hq q scales in qsc
+  float qsc[kMaxQScales];  // FP8-domain attention: q_scale per tensor / per q head
 };
 
 

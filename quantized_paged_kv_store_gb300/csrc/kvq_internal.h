@@ -95,14 +95,24 @@ struct DecodePlan {
 };
 
 // Fills `plan` for a call; returns false (with a message) if unsupported.
+// qf8: the FP8-domain attention kernel (FP8 caches only) will be launched.
 bool plan_decode(const Geometry& g, int batch, int num_q_heads, int max_pages_per_seq,
-                 int device, DecodePlan* plan, const char** why);
+                 int device, DecodePlan* plan, const char** why, bool qf8 = false);
 
+// q_scales (host, num_q_scales = 1 or num_q_heads, <= 256) selects FP8-domain
+// attention with the query quantized to E4M3; nullptr: the bf16 query path.
 cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePlan& plan,
                           const void* q, int num_q_heads, const int32_t* page_table,
                           int max_pages_per_seq, const int32_t* seq_lens, int batch,
                           float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
                           const int32_t* pt_rows, int pt_nrows, void* out, void* workspace,
-                          int* err, cudaStream_t stream);
+                          int* err, cudaStream_t stream, const float* q_scales = nullptr,
+                          int num_q_scales = 0);
+
+// E4M3 codes of a bf16 query [rows][num_q_heads][head_dim] quantized with
+// q_scales (host, 1 or num_q_heads, <= 256): the FP8-domain attention's rule.
+cudaError_t launch_quantize_query(const void* q, int64_t rows, int num_q_heads, int head_dim,
+                                  const float* q_scales, int num_q_scales, void* codes,
+                                  cudaStream_t stream);
 
 }  // namespace kvq

@@ -16,6 +16,7 @@
 #include <algorithm>
 
 #include "kvq_codecs.cuh"
+#include "kvq_decode_args.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -54,66 +55,6 @@ __device__ __forceinline__ uint32_t block_amax_bits(const uint32_t w[8]) {
   const uint32_t lo = m & 0x7FFFu, hi = (m >> 16) & 0x7FFFu;
   // NaN patterns are larger than every finite magnitude and +inf as integers
   return (lo > hi ? lo : hi) << 16;
-}
-
-// Packed fp32 pairs (sm_100 family f32x2 arithmetic): each op rounds both
-// halves exactly as its scalar counterpart (round to nearest, subnormals kept).
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
-// Correctly rounded x / s from r = RN(1 / s), by P. Markstein's method
-// ("Computation of elementary functions on the IBM RISC System/6000
-// processor", IBM J. Res. Dev. 34(1), 1990): q = RN(x r) is within 1.5 ulp;
-// one correction q + r (x - s q) (residual exact with a fused multiply-add)
-// makes it faithful, and by Markstein's theorem a second correction from a
-// faithful quotient yields RN(x / s).  Requires a finite quotient (the callers
-// bound the block maximum times r).  The residual is exact unless it underflows,
-// which with s in [2^-89, 2^80] happens only for quotients below 2^-14; there the
-// correction is off by less than 2^-60, far from every rounding decision of the
-// target codes (the smallest, 2^-17, is E5M2's half subnormal).  The residual is
-// formed as s q - x so that signed zeros keep their sign.
-__device__ __forceinline__ float div_rn_markstein(float x, float s, float r) {
-  float q = x * r;
-  float e = fmaf(s, q, -x);
-  q = fmaf(-e, r, q);
-  e = fmaf(s, q, -x);
-  return fmaf(-e, r, q);
-}
-
-// The same two corrections on a pair of quotients x / s.  S2 = {s, s},
-// R2 = {r, r}, NR2 = {-r, -r}: -e * r is formed as e * (-r) (the same
-// product), and -x as x * (-1) + (-0), exact and with the sign of zero
-// flipped as a negation does.
-__device__ __forceinline__ uint64_t div2_rn_markstein(uint64_t x, uint64_t S2, uint64_t R2,
-                                                      uint64_t NR2) {
-  const uint64_t kMinusOne = 0xBF800000BF800000ull, kMinusZero = 0x8000000080000000ull;
-  const uint64_t nx = f2_fma(x, kMinusOne, kMinusZero);
-  uint64_t q = f2_mul(x, R2);
-  uint64_t e = f2_fma(S2, q, nx);
-  q = f2_fma(e, NR2, q);
-  e = f2_fma(S2, q, nx);
-  return f2_fma(e, NR2, q);
-}
-
-// Two bf16 values of a word as a pair of fp32 (low element in the low half).
-__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
-  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 // Four bytes (the low byte of each word) into one word, c0 lowest.
@@ -571,6 +512,64 @@ cudaError_t launch_dequantize(const Geometry& g, const LayerView& L, const int64
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------
+// Query quantization of FP8-domain attention ("Quantized KV cache" (vLLM),
+// FP8 KV cache overview: with an FP8 cache the attention can run in the FP8
+// domain, the query quantized to FP8 too; Supported schemes: q_scale per
+// tensor or per attention head).  One thread per 16 consecutive elements.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct QuantQueryArgs {
+  const uint16_t* q;  // [rows][Hq][D] bf16
+  uint8_t* codes;     // [rows][Hq][D]
+  int64_t items;      // rows * Hq * D / 16
+  int Hq, nb;         // q heads, 16-element blocks per head row
+  int nqs;            // 1 or Hq
+  float qs[kMaxQScales];
+};
+
+__global__ void __launch_bounds__(256) quantize_query_kernel(QuantQueryArgs a) {
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < a.items;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int head = (int)((it / a.nb) % a.Hq);
+    const float s = a.qs[a.nqs == 1 ? 0 : head];
+    const float rs = 1.0f / s;
+    const uint4* src = reinterpret_cast<const uint4*>(a.q + it * 16);
+    const uint4 lo = __ldg(src), hi = __ldg(src + 1);
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t m2 = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(w[i]));
+    const float amax = __uint_as_float(max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu) << 16);
+    const bool fast = s >= 0x1p-80f && s <= 0x1p80f && amax * rs < 1e37f;  // NaN: false
+    uint32_t c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      c[i] = quant2_e4m3(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u), s, rs, fast);
+    *reinterpret_cast<uint4*>(a.codes + it * 16) =
+        make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_query(const void* q, int64_t rows, int num_q_heads, int head_dim,
+                                  const float* q_scales, int num_q_scales, void* codes,
+                                  cudaStream_t stream) {
+  QuantQueryArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.codes = static_cast<uint8_t*>(codes);
+  a.nb = head_dim / 16;
+  a.Hq = num_q_heads;
+  a.items = rows * num_q_heads * a.nb;
+  a.nqs = num_q_scales;
+  for (int i = 0; i < kMaxQScales; ++i) a.qs[i] = i < num_q_scales ? q_scales[i] : 1.0f;
+  if (a.items == 0) return cudaSuccess;
+  quantize_query_kernel<<<grid_for(a.items), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 // ---------------------------------------------------------------------------
 // Per-head scales and calibration ("Quantized KV cache" (vLLM features page):

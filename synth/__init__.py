@@ -172,6 +172,14 @@ class Workload:
             self._scales[key] = self._amax_of(ks, vs)
         return self._scales_of(self._scales[key], fmt)
 
+    def q_scales(self, layer: int = 0, per_head: bool = False, step: int = 0) -> np.ndarray:
+        """FP8-domain attention query scales by the same recipe: amax of the
+        query (bf16 values) over the batch / 448, per tensor ([1]) or per q
+        head ([Hq]); 1.0 where the amax is 0."""
+        q = np.abs(bf16_bits_to_float(self.q(layer, step)))
+        a = q.max(axis=(0, 2)) if per_head else np.array([q.max()])
+        return np.where(a > 0, a / np.float32(448.0), 1.0).astype(np.float32)
+
     def scales(self, layer: int = 0) -> np.ndarray:
         """float32 [2]: FP8 {k_scale, v_scale} or NVFP4 {g_k, g_v} = amax / format max,
         amax taken over every generated K (resp. V) value of the layer; 1.0 otherwise
