@@ -206,11 +206,16 @@ kvq_status kvq_decode_attention(kvq_cache* cache, int layer, const void* q_bf16,
  *   q_seq, q_len:     int32 [num_q_tokens] device arrays; 0 <= q_seq[i] <
  *                     num_seqs, 0 <= q_len[i] <= max_pages_per_seq * page_size.
  *   page_table:       int32 [num_seqs][max_pages_per_seq].
- *   workspace, workspace_bytes: not used (kept for the signature; may be
- *                     NULL / 0).
- * Every K/V tile of a sequence is read and dequantized once per 64 (query,
- * q head) rows of a kv head, shared by those rows' queries (a chunk of 8
- * queries at 8 q heads per kv head).  Out-of-range
+ *   workspace:        device scratch, 16-byte aligned, of
+ *                     kvq_extend_workspace_size(...) bytes for the fastest
+ *                     plan: each sequence's context is split across CTAs and
+ *                     the splits' partial outputs are merged.  A smaller
+ *                     workspace (or NULL / 0) is valid: the call then uses
+ *                     fewer splits (none without a workspace).
+ * Every K/V chunk of a sequence is read and dequantized once per 128 (query,
+ * q head) rows of a kv head, shared by those rows' queries (16 queries at 8 q
+ * heads per kv head); QK^T and PV run on the tcgen05 tensor cores with fp32
+ * accumulators in tensor memory.  Out-of-range
  * q_seq, q_len or page ids raise KVQ_ERR_DEVICE_RANGE in the device error word
  * and zero that query's output.  Other rules and errors as for
  * kvq_decode_attention.
@@ -260,6 +265,11 @@ kvq_status kvq_decode_attention_fp8q(kvq_cache* cache, int layer, const void* q_
 kvq_status kvq_quantize_query(const void* q_bf16, int rows, int num_q_heads, int head_dim,
                               const float* q_scales, int num_q_scales, void* q_codes,
                               kvq_stream stream);
+
+/* Bytes of workspace kvq_extend_attention uses at most for these sizes (0 when
+ * it needs none, or on invalid arguments; see kvq_last_error_string). */
+size_t kvq_extend_workspace_size(const kvq_cache* cache, int num_q_tokens, int num_q_heads,
+                                 int max_pages_per_seq);
 
 /* Bytes of workspace kvq_decode_attention needs for these sizes (0 on invalid
  * arguments; see kvq_last_error_string). */

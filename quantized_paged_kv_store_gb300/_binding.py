@@ -35,6 +35,7 @@ def _load():
         "kvq_layer_head_scales": ([vp, i32, ctypes.POINTER(f32), ctypes.POINTER(f32), vp], i32),
         "kvq_decode_attention": ([vp, i32, vp, i32, vp, i32, vp, i32, f32, vp, vp, sz, vp], i32),
         "kvq_decode_workspace_size": ([vp, i32, i32, i32], sz),
+        "kvq_extend_workspace_size": ([vp, i32, i32, i32], sz),
         "kvq_decode_attention_fp8q": ([vp, i32, vp, i32, ctypes.POINTER(f32), i32, vp, i32, vp, i32,
                                        f32, vp, vp, sz, vp], i32),
         "kvq_quantize_query": ([vp, i32, i32, i32, ctypes.POINTER(f32), i32, vp, vp], i32),
@@ -208,6 +209,12 @@ def kvq_extend_attention(handle, layer, q, q_seq, q_len, page_table, sm_scale, o
                                     _stream(stream)), "kvq_extend_attention")
 
 
+def kvq_extend_workspace_size(handle, num_q_tokens, num_q_heads, max_pages_per_seq) -> int:
+    """Workspace bytes of the fastest extend plan (0: none needed)."""
+    return lib.kvq_extend_workspace_size(ctypes.c_void_p(handle), num_q_tokens, num_q_heads,
+                                         max_pages_per_seq)
+
+
 def kvq_decode_attention_noalloc(handle, layer, q, page_table, seq_lens, sm_scale, out,
                                  stream=None):
     """kvq_decode_attention with the library's static scratch instead of a
@@ -312,8 +319,8 @@ class KVQCache:
         if out is None:
             out = torch.empty_like(q)
         if workspace is None:
-            n = self.workspace_size(q.shape[0], q.shape[1], page_table.shape[1])
-            workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+            n = kvq_extend_workspace_size(self.handle, q.shape[0], q.shape[1], page_table.shape[1])
+            workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
         kvq_extend_attention(self.handle, layer, q, q_seq, q_len, page_table, sm_scale, out,
                              workspace, stream)
         return out

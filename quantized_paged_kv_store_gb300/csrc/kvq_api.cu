@@ -574,13 +574,22 @@ kvq_status kvq_quantize_query(const void* q_bf16, int rows, int num_q_heads, int
   return KVQ_OK;
 }
 
+size_t kvq_extend_workspace_size(const kvq_cache* c, int num_q_tokens, int num_q_heads,
+                                 int max_pages_per_seq) {
+  if (!c || num_q_tokens < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0 ||
+      num_q_heads % c->geo.kv_heads != 0) {
+    fail(KVQ_ERR_INVALID_ARG, "invalid arguments to kvq_extend_workspace_size");
+    return 0;
+  }
+  const int splits = kvq::extend_splits(c->geo, num_q_tokens, num_q_heads, max_pages_per_seq, c->device);
+  return kvq::extend_workspace_bytes(splits, num_q_tokens, num_q_heads);
+}
+
 kvq_status kvq_extend_attention(kvq_cache* c, int layer, const void* q_bf16, int num_q_heads,
                                 int num_q_tokens, const int32_t* q_seq, const int32_t* q_len,
                                 const int32_t* page_table, int num_seqs, int max_pages_per_seq,
                                 float sm_scale, void* out_bf16, void* workspace,
                                 size_t workspace_bytes, kvq_stream stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   kvq_status st = check_layer(c, layer);
   if (st) return st;
   const kvq::Geometry& g = c->geo;
@@ -596,14 +605,20 @@ kvq_status kvq_extend_attention(kvq_cache* c, int layer, const void* q_bf16, int
   if (num_q_tokens == 0) return KVQ_OK;
   if (!q_bf16 || !q_seq || !q_len || !page_table || !out_bf16)
     return fail(KVQ_ERR_INVALID_ARG, "NULL device pointer");
-  if (!aligned16(q_bf16) || !aligned16(out_bf16))
-    return fail(KVQ_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (!aligned16(q_bf16) || !aligned16(out_bf16) || (workspace && !aligned16(workspace)))
+    return fail(KVQ_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
   if ((st = check_device(c))) return st;
+  // context splits: as many as the plan wants and the workspace holds
+  int splits = kvq::extend_splits(g, num_q_tokens, num_q_heads, max_pages_per_seq, c->device);
+  while (splits > 1 && (!workspace ||
+                        kvq::extend_workspace_bytes(splits, num_q_tokens, num_q_heads) > workspace_bytes))
+    --splits;
   float kf, vf;
   tensor_scales(c, layer, &kf, &vf);
   cudaError_t e = kvq::launch_extend(g, view(c, layer), q_bf16, num_q_heads, num_q_tokens, q_seq,
                                      q_len, page_table, num_seqs, max_pages_per_seq, sm_scale, kf, vf,
-                                     head_scales(c, layer), out_bf16, c->err, (cudaStream_t)stream);
+                                     head_scales(c, layer), out_bf16, c->err, splits, workspace,
+                                     (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "extend attention launch");
   return KVQ_OK;
 }

@@ -1,40 +1,81 @@
-// kvq_extend.cu -- extend (chunked-prefill) attention over the quantized cache.
+// kvq_extend.cu -- extend (chunked-prefill) attention over the quantized cache
+// on the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // "SGLang PR #21954 analysis: NVFP4 KV cache", Code analysis 1: the prefill /
 // extend path reads the previously stored, quantized KV (there through a
-// dequantized workspace; here dequantized in place, once per K/V tile for all
-// the queries that share it, as "Quantized KV Cache" (SGLang documentation),
-// performance warning, asks of an attention kernel).
+// dequantized workspace; here dequantized in shared memory once per K/V chunk
+// for all the queries that share it, as "Quantized KV Cache" (SGLang
+// documentation), performance warning, asks of an attention kernel).
 //
 // Query token i of sequence q_seq[i] attends to that sequence's tokens
-// [0, q_len[i]).  Rows are (query, q head) pairs laid out query-major; a CTA of
-// four warps owns 64 consecutive rows of one kv head (8 queries at G = 8) and
-// walks the K/V tiles of their sequence once:
-//   - the raw rows of each 16-token tile are copied into shared memory with
-//     cp.async, four tiles in flight (absent tokens and bad pages zero-filled);
-//   - every thread dequantizes one 16-element block of K and one of V per tile
-//     into a shared f16 tile (FP8 / NVFP4, exact) or bf16 tile (bf16 / FP4
-//     block-16, exact: E2M1 x 2^(E-127) fits bf16's range);
-//   - each warp computes S = Q K^T for its 16 rows with mma.sync.m16n8k16
-//     (K fragments by ldmatrix), an online softmax per row (base 2, lazy
-//     rescale when a row's maximum grows by more than 2^8), and O += P V
-//     (P reused from the S accumulators, V fragments by ldmatrix.trans; for the
-//     bf16 instances P is split into high and low bf16 parts).
+// [0, q_len[i]).  Rows are (query, q head) pairs laid out query-major; a CTA
+// of four warps owns 128 consecutive rows of one kv head (16 queries at 8 q
+// heads per kv head) -- one row per thread and per tensor-memory lane -- and
+// one split of the context (gridDim.z splits; their partial outputs and
+// log-sum-exps are merged by extend_merge_kernel).  Per 64-token chunk:
+//   - lanes of warp 0 bulk-copy the raw K/V rows (and block scales) of the
+//     chunk's four 16-token (page, kv head) slabs into a two-stage ring,
+//     completing on an mbarrier;
+//   - every thread dequantizes half a token row of K and of V into f16 (FP8,
+//     NVFP4) or bf16 (bf16, FP4 block-16) tiles in the 128-byte-swizzled
+//     layout the tensor cores read (exact for every format: the per-tensor /
+//     global scale stays out and is applied to the logits and the output);
+//   - one thread issues S = Q K^T (M = 128 rows, N = 64 tokens, K = 128 in
+//     eight tcgen05.mma kind::f16 steps, fp32 accumulators in tensor memory;
+//     Q in f16 is scaled per row by a power of two that keeps it exact) and
+//     commits to an mbarrier;
+//   - each thread loads its row of S from tensor memory, runs the online
+//     softmax (base 2, lazy rescale when its maximum grows by more than 2^8,
+//     causal mask by q_len) and stores P back to tensor memory in f16 (or, for
+//     the bf16 operand formats, as a high and a low bf16 part: P = hi + lo to
+//     ~2^-16);
+//   - one thread issues O += P V (A = P from tensor memory, B = V in the
+//     MN-major swizzled layout, two 64-column halves of head_dim).
 // Rows of different sequences inside one CTA take one pass per distinct
-// sequence (the other rows masked).  No split-K: the output is written once.
+// sequence (the other rows masked).  Every wait is bounded; a wait that runs
+// out records KVQ_ERR_TIMEOUT and the CTA stops issuing work.
 #include "kvq_codecs.cuh"
 #include "kvq_decode_args.cuh"
 #include "kvq_internal.h"
 
+#include <algorithm>
+
 namespace kvq {
 namespace {
 
-constexpr int kXWarps = 4;
-constexpr int kXThreads = 32 * kXWarps;
-constexpr int kXRows = 16 * kXWarps;           // (query, q head) rows per CTA
-constexpr int kXStride = kHeadDim * 2 + 16;    // bytes per shared row (pad: conflict-free ldmatrix)
-constexpr int kXTile = kTile * kXStride;       // one dequantized K (or V) tile
-static_assert(kXThreads == kTile * (kHeadDim / 16), "one 16-element block per thread per tile");
+constexpr int kXRows = 128;        // (query, q head) rows per CTA = TMEM lanes
+constexpr int kXThreads = 128;
+constexpr int kChunk = 64;         // tokens per chunk (four 16-token tiles)
+constexpr int kMaxSplits = 16;
+constexpr uint32_t kXWaitLimit = 1u << 22;
+
+// tensor-memory columns
+constexpr uint32_t kColS = 0;      // S: 64 fp32 columns
+constexpr uint32_t kColO = 64;     // O: 128 fp32 columns (two halves of head_dim)
+constexpr uint32_t kColPh = 192;   // P high bf16 part: 32 columns (bf16x2)
+constexpr uint32_t kColPl = 224;   // P low part
+constexpr uint32_t kTmemCols = 256;
+
+// shared memory (dynamic, 1024-byte aligned offsets)
+constexpr int kSQ = 0;                        // Q: 2 K-atoms x 128 rows x 128 B
+constexpr int kSK = kSQ + 2 * kXRows * 128;   // K: 2 atoms x 64 tokens x 128 B
+constexpr int kSV = kSK + 2 * kChunk * 128;   // V: same layout, read MN-major
+constexpr int kSRaw = kSV + 2 * kChunk * 128; // raw stages
+
+template <kvq_format F>
+struct XTraits {
+  static constexpr int kRow = (F == KVQ_BF16) ? 256 : (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) ? 128 : 64;
+  static constexpr bool kScales = (F == KVQ_FP4_BLOCK16 || F == KVQ_NVFP4);
+  // f16 operands (FP8 and NVFP4 values are exact in f16; Q prescaled per row
+  // by a power of two; P one f16 part); bf16 operands with P split into a
+  // high and a low part for the bf16 and FP4 block-16 caches
+  static constexpr bool kF16 = (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2 || F == KVQ_NVFP4);
+  // raw stage: K rows of 64 tokens, V rows, K scale rows, V scale rows
+  static constexpr int kData = kChunk * kRow;
+  static constexpr int kScl = kScales ? kChunk * 8 : 0;
+  static constexpr int kStage = 2 * kData + 2 * kScl;
+  static constexpr int kSmem = kSRaw + 2 * kStage + 1024;  // + alignment slack
+};
 
 struct ExtendArgs {
   const uint16_t* q;         // [n][Hq][128] bf16
@@ -53,56 +94,97 @@ struct ExtendArgs {
   const float* kfac;         // per-kv-head K / V scales, or null
   const float* vfac;
   int* err;
+  int splits;                // context splits (gridDim.z)
+  float* part_o;             // splits > 1: [n * Hq][splits][128]
+  float* part_lse;           // splits > 1: [n * Hq][splits] (log2 units)
 };
 
-template <kvq_format F>
-struct XTraits {
-  static constexpr bool kBf16 = (F == KVQ_BF16 || F == KVQ_FP4_BLOCK16);  // bf16 mma
-  static constexpr int kRow = (F == KVQ_BF16) ? 256 : (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) ? 128 : 64;
-  static constexpr int kBlk = kRow / 8;  // bytes of one 16-element block
-  static constexpr bool kScales = (F == KVQ_FP4_BLOCK16 || F == KVQ_NVFP4);
-  // raw bytes of one tile as copied: K rows, V rows, K scale rows, V scale rows
-  static constexpr int kStageBytes = 2 * kTile * kRow + 2 * kTile * 8;
-  static constexpr int kCopies = 2 * kRow + (kScales ? 2 * kTile : 0);  // 16 B data + 8 B scale copies
-};
-constexpr int kXStages = 4;  // raw tiles in flight per CTA
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  uint32_t polls = 0;
+  bool ok = mbar_try_wait(bar, parity);
+  while (!ok && ++polls < kXWaitLimit) ok = mbar_try_wait(bar, parity);
+  return ok;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Raw bytes of one 16-element block (K or V) held between load and dequant.
-struct RawBlock {
-  uint4 a, b;   // data (bf16: 32 B; fp8: a = 16 B; fp4: a.x, a.y = 8 B)
-  uint32_t sc;  // block scale byte (FP4 formats)
-};
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand: start
+// address, leading / stride byte offsets (the stride is the distance between
+// 8-row groups), descriptor version 1 (bits 46-48), layout 2 = 128B swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;  // leading byte offset 16 (unused by these layouts)
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both bf16
+// (bf = 1) or both f16 (bf = 0), A K-major, B K-major (b_mn = 0) or MN-major
+// (1), N and M.
+__host__ __device__ constexpr uint32_t idesc_16(uint32_t bf, uint32_t n, uint32_t m, uint32_t b_mn) {
+  return (1u << 4) | (bf << 7) | (bf << 10) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+               :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
-template <bool BF16>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  if (BF16)
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  else
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
+
+// 32 consecutive 32-bit tensor-memory columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+               "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                 "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+                 "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+                 "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+                 "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+                 "=r"(v[31])
+               : "r"(taddr) : "memory");
 }
-__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+               "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                  "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+                  "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+                  "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+                  "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]),
+                  "r"(v[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t bf2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
@@ -118,93 +200,88 @@ __device__ __forceinline__ float ex2x(float x) {
   return r;
 }
 
-// Asynchronous global -> shared copies (cp.async); a copy of `valid` false
-// reads nothing and fills the destination with zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
-               "r"(valid ? 8 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Offset of 16-byte chunk c (0..7) of row `row` in a 128B-swizzled atom.
+__device__ __forceinline__ uint32_t sw_off(int row, int c) { return (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4)); }
 
-// The raw block (tile token tok, block blk) of K (kv = 0) or V from a raw stage.
+// Dequantizes half a token row (64 head_dim elements, half hf) of K or V from
+// the raw stage into 32 packed pairs -- f16x2 for the FP8 and NVFP4 caches,
+// bf16x2 for the others -- exactly; the per-tensor / global scale is not
+// applied (it multiplies the logits or the output).
 template <kvq_format F>
-__device__ __forceinline__ RawBlock raw_block(const uint8_t* stage, int kv, int tok, int blk) {
+__device__ __forceinline__ void dequant_half(const uint8_t* data, const uint8_t* scl, int tt, int hf,
+                                             uint32_t (&o)[32]) {
   using Tr = XTraits<F>;
-  RawBlock rb;
-  const uint8_t* p = stage + kv * kTile * Tr::kRow + tok * Tr::kRow + blk * Tr::kBlk;
+  const uint8_t* row = data + tt * Tr::kRow + hf * (Tr::kRow / 2);
   if (F == KVQ_BF16) {
-    rb.a = reinterpret_cast<const uint4*>(p)[0];
-    rb.b = reinterpret_cast<const uint4*>(p)[1];
-  } else if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
-    rb.a = reinterpret_cast<const uint4*>(p)[0];
-  } else {
-    const uint2 v = reinterpret_cast<const uint2*>(p)[0];
-    rb.a.x = v.x;
-    rb.a.y = v.y;
-    rb.sc = stage[2 * kTile * Tr::kRow + kv * kTile * 8 + tok * 8 + blk];
-  }
-  return rb;
-}
-
-// Dequantizes one block into 8 packed pairs (f16x2, or bf16x2 for the bf16
-// instances); exact for every format.
-template <kvq_format F>
-__device__ __forceinline__ void dequant_block(const RawBlock& rb, uint32_t (&o)[8]) {
-  if (F == KVQ_BF16) {
-    o[0] = rb.a.x; o[1] = rb.a.y; o[2] = rb.a.z; o[3] = rb.a.w;
-    o[4] = rb.b.x; o[5] = rb.b.y; o[6] = rb.b.z; o[7] = rb.b.w;
-  } else if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
-    const uint32_t w[4] = {rb.a.x, rb.a.y, rb.a.z, rb.a.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      o[2 * i] = (F == KVQ_FP8_E4M3) ? dec2_e4m3_h2(w[i]) : dec2_e5m2_h2(w[i]);
-      o[2 * i + 1] = (F == KVQ_FP8_E4M3) ? dec2_e4m3_h2_hi(w[i]) : dec2_e5m2_h2_hi(w[i]);
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = reinterpret_cast<const uint4*>(row)[c];
+      o[4 * c] = v.x; o[4 * c + 1] = v.y; o[4 * c + 2] = v.z; o[4 * c + 3] = v.w;
+    }
+  } else if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = reinterpret_cast<const uint4*>(row)[c];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // E4M3 and E5M2 values are exact in f16
+        o[8 * c + 2 * i] = (F == KVQ_FP8_E4M3) ? dec2_e4m3_h2(w[i]) : dec2_e5m2_h2(w[i]);
+        o[8 * c + 2 * i + 1] = (F == KVQ_FP8_E4M3) ? dec2_e4m3_h2_hi(w[i]) : dec2_e5m2_h2_hi(w[i]);
+      }
     }
   } else {
-    uint32_t h[8];  // E2M1 pairs as f16x2 (even element low)
-    h[0] = dec2_e2m1_h2<0>(rb.a.x); h[1] = dec2_e2m1_h2<1>(rb.a.x);
-    h[2] = dec2_e2m1_h2<2>(rb.a.x); h[3] = dec2_e2m1_h2<3>(rb.a.x);
-    h[4] = dec2_e2m1_h2<0>(rb.a.y); h[5] = dec2_e2m1_h2<1>(rb.a.y);
-    h[6] = dec2_e2m1_h2<2>(rb.a.y); h[7] = dec2_e2m1_h2<3>(rb.a.y);
-    if (F == KVQ_NVFP4) {  // E2M1 x E4M3 is exact in f16
-      const uint32_t s2 = dec2_e4m3_h2(rb.sc | (rb.sc << 8));
+    const uint4 v0 = reinterpret_cast<const uint4*>(row)[0], v1 = reinterpret_cast<const uint4*>(row)[1];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scl + tt * 8 + hf * 4);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = hmul2x(h[i], s2);
-    } else {  // E2M1 x 2^(E - 127), exact in fp32 and in bf16
-      const float m = exp2i((int)(rb.sc & 0xFF) - 127);
+    for (int blk = 0; blk < 4; ++blk) {
+      const uint32_t sc = (sc4 >> (8 * blk)) & 0xFF;
+      const uint32_t wa = w[2 * blk], wb = w[2 * blk + 1];
+      uint32_t h[8] = {dec2_e2m1_h2<0>(wa), dec2_e2m1_h2<1>(wa), dec2_e2m1_h2<2>(wa), dec2_e2m1_h2<3>(wa),
+                       dec2_e2m1_h2<0>(wb), dec2_e2m1_h2<1>(wb), dec2_e2m1_h2<2>(wb), dec2_e2m1_h2<3>(wb)};
+      if (F == KVQ_NVFP4) {
+        // E2M1 x E4M3 block scale: exact in f16 (at most 2688, at least 2^-10)
+        const uint32_t s2 = dec2_e4m3_h2(sc | (sc << 8));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = pack_bf2(h2_lo(h[i]) * m, h2_hi(h[i]) * m);
+        for (int i = 0; i < 8; ++i) o[8 * blk + i] = hmul2x(h[i], s2);
+      } else {
+        // E2M1 x 2^(E - 127): exact in fp32 and in bf16
+        const float m = exp2i((int)sc - 127);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[8 * blk + i] = bf2(h2_lo(h[i]) * m, h2_hi(h[i]) * m);
+      }
     }
   }
 }
 
 template <kvq_format F>
-__global__ void __launch_bounds__(kXThreads, 4) extend_kernel(ExtendArgs a) {
+__global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   using Tr = XTraits<F>;
-  constexpr bool BF = Tr::kBf16;
-  __shared__ __align__(128) uint8_t sraw[kXStages][Tr::kStageBytes];  // raw tiles in flight
-  __shared__ __align__(128) uint8_t sm[2][kXTile];                     // dequantized [K|V] tile
-  __shared__ int row_seq[kXRows];                        // sequence of each row, -1: done / none
+  extern __shared__ uint8_t xsm_raw[];
+  __shared__ __align__(8) uint64_t bars[4];  // raw stage 0, raw stage 1, S ready, O ready
+  __shared__ uint32_t tmem_slot;
+  __shared__ int row_seq[kXRows];
   __shared__ int row_len[kXRows];
-  __shared__ int pass_seq, pass_max, pass_bad;
+  __shared__ int pass_seq, pass_max, pass_bad, dead;
+  __shared__ uint32_t stage_ok[2];  // per raw stage: bit t set if tile t was copied
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r4 = lane >> 2, c = lane & 3;
-  const int h = blockIdx.y;
+  const int h = blockIdx.y, split = blockIdx.z;
   const long long R0 = (long long)blockIdx.x * kXRows;
+  const uint32_t base_u32 = smem_u32(xsm_raw);
+  uint8_t* sm = xsm_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
+  const uint32_t sm_u32 = smem_u32(sm);
+  const uint32_t bar_raw0 = smem_u32(&bars[0]), bar_s = smem_u32(&bars[2]), bar_o = smem_u32(&bars[3]);
 
-  // ---- rows of this CTA: (query, head) = divmod(R0 + rho, G) ----------------
-  for (int rho = tid; rho < kXRows; rho += kXThreads) {
-    const long long R = R0 + rho;
-    const long long qi = R / a.G;
+  // ---- rows of this CTA: (query, q head) = divmod(R0 + tid, G) ----------------
+  const long long R = R0 + tid;
+  const long long qi = R / a.G;
+  const bool qvalid = qi < a.n;
+  const int qhead = h * a.G + (int)(R % a.G);
+  {
     int s = -1, T = 0;
-    if (qi < a.n) {
+    if (qvalid) {
       s = __ldg(a.q_seq + qi);
       T = __ldg(a.q_len + qi);
       if (s < 0 || s >= a.S || T < 0 || T > a.max_pages * a.P) {
@@ -212,88 +289,77 @@ __global__ void __launch_bounds__(kXThreads, 4) extend_kernel(ExtendArgs a) {
         s = -2;  // invalid: output zeros
       }
     }
-    row_seq[rho] = s;
-    row_len[rho] = T;
+    row_seq[tid] = s;
+    row_len[tid] = T;
   }
-
-  // ---- this thread's two rows: warp rows r4 and r4 + 8 ----------------------
-  long long qrow[2];
-  int qhead[2];
-  bool qvalid[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const long long R = R0 + warp * 16 + r4 + 8 * i;
-    qrow[i] = R / a.G;
-    qhead[i] = h * a.G + (int)(R % a.G);
-    qvalid[i] = qrow[i] < a.n;
-  }
-  // Q fragments (A operand): k-step ks covers d = 16 ks .. 16 ks + 15; this
-  // thread holds d = 16 ks + 2c, +1 and 16 ks + 2c + 8, +9 of both rows.
-  uint32_t qa[8][4];
-  float cs[2];
+  // ---- Q row -> 128B-swizzled K-major tile (two 64-element K atoms); for the
+  // f16 operand formats the row is scaled by 2^-sq so that its largest
+  // magnitude lies in [2^14, 2^15) and every bf16 value of it is exact in f16
+  // (2^sq joins the row's logit scale) ----------------------------------------
+  float qmul = 1.f;
   {
-    float qf[2][32];
+    const uint4* src = reinterpret_cast<const uint4*>(a.q + ((qvalid ? qi : 0) * a.Hq + qhead) * kHeadDim);
+    uint4 qv[16];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(
-          a.q + ((qvalid[i] ? qrow[i] : 0) * a.Hq + qhead[i]) * kHeadDim);
+    for (int c = 0; c < 16; ++c) qv[c] = qvalid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (Tr::kF16) {
+      uint32_t m2 = 0u;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t w0 = qvalid[i] ? __ldg(src + 8 * ks + c) : 0u;
-        const uint32_t w1 = qvalid[i] ? __ldg(src + 8 * ks + 4 + c) : 0u;
-        qf[i][4 * ks + 0] = bf16_bits_to_float(w0 & 0xFFFF);
-        qf[i][4 * ks + 1] = bf16_bits_to_float(w0 >> 16);
-        qf[i][4 * ks + 2] = bf16_bits_to_float(w1 & 0xFFFF);
-        qf[i][4 * ks + 3] = bf16_bits_to_float(w1 >> 16);
+      for (int c = 0; c < 16; ++c) {
+        asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(qv[c].x));
+        asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(qv[c].y));
+        asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(qv[c].z));
+        asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(qv[c].w));
+      }
+      const float amax = __uint_as_float(max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu) << 16);
+      const int sq = (amax > 0.f && amax < INFINITY) ? max(-126, min(126, floor_log2(amax) - 14)) : 0;
+      const float mul = exp2i(-sq);
+      qmul = exp2i(sq);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t w[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+        uint32_t hv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t r;
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;"
+              : "=r"(r) : "f"(bf16_bits_to_float(w[i] >> 16) * mul), "f"(bf16_bits_to_float(w[i] & 0xFFFF) * mul));
+          hv[i] = r;
+        }
+        qv[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
       }
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float hf = a.kfac ? a.qscale * __ldg(a.kfac + h) : a.qscale;
-      if (BF) {
-        cs[i] = hf;
-      } else {
-        // power-of-two prescale: max |q'| in [2^14, 2^15) keeps bf16 values exact in f16
-        float amax = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qf[i][j]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const int sq = amax > 0.f ? max(-126, min(126, floor_log2(amax) - 14)) : 0;
-        const float mul = exp2i(-sq);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) qf[i][j] *= mul;
-        cs[i] = hf * exp2i(sq);
-      }
-    }
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      if (BF) {
-        qa[ks][0] = pack_bf2(qf[0][4 * ks], qf[0][4 * ks + 1]);
-        qa[ks][1] = pack_bf2(qf[1][4 * ks], qf[1][4 * ks + 1]);
-        qa[ks][2] = pack_bf2(qf[0][4 * ks + 2], qf[0][4 * ks + 3]);
-        qa[ks][3] = pack_bf2(qf[1][4 * ks + 2], qf[1][4 * ks + 3]);
-      } else {
-        qa[ks][0] = pack_h2(qf[0][4 * ks], qf[0][4 * ks + 1]);
-        qa[ks][1] = pack_h2(qf[1][4 * ks], qf[1][4 * ks + 1]);
-        qa[ks][2] = pack_h2(qf[0][4 * ks + 2], qf[0][4 * ks + 3]);
-        qa[ks][3] = pack_h2(qf[1][4 * ks + 2], qf[1][4 * ks + 3]);
-      }
-    }
+    for (int c = 0; c < 16; ++c)
+      *reinterpret_cast<uint4*>(sm + kSQ + (c >> 3) * (kXRows * 128) + sw_off(tid, c & 7)) = qv[c];
   }
-
-  float o[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  bool poison[2] = {false, false};
-
-  const int my_tok = tid >> 3, my_blk = tid & 7;  // the block this thread loads per tile
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(&sm[0][0]);
-  const uint32_t sraw_base = (uint32_t)__cvta_generic_to_shared(&sraw[0][0]);
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    dead = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(&tmem_slot)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_proxy_async();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
 
-  // ---- one pass per distinct sequence among the CTA's rows ----------------------
+  const float cs = (a.kfac ? a.qscale * __ldg(a.kfac + h) : a.qscale) * qmul;
+  const float vf = a.vfac ? __ldg(a.vfac + h) : a.v_factor;
+  constexpr uint32_t kBf = Tr::kF16 ? 0u : 1u;
+  constexpr uint32_t kIdQK = idesc_16(kBf, kChunk, kXRows, 0);
+  constexpr uint32_t kIdPV = idesc_16(kBf, 64, kXRows, 1);
+
+  uint32_t n_raw_issued = 0, n_raw_used = 0, n_s = 0, n_o = 0;
+  bool row_done = false;
+
+  // ---- one pass per distinct sequence among the CTA's rows -------------------
   for (;;) {
     if (tid == 0) {
       int s = -1;
@@ -307,209 +373,379 @@ __global__ void __launch_bounds__(kXThreads, 4) extend_kernel(ExtendArgs a) {
     }
     __syncthreads();
     const int s = pass_seq;
-    if (s < 0) break;
+    if (s < 0 || dead) break;
     const int maxT = pass_max;
-    bool act[2];
-    int Tr_[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int rho = warp * 16 + r4 + 8 * i;
-      act[i] = row_seq[rho] == s;
-      Tr_[i] = row_len[rho];
-    }
+    const bool act = row_seq[tid] == s;
+    const int Tr_ = row_len[tid];
     const int32_t* prow = a.page_table + (long long)s * a.max_pages;
-    const int ntiles = (maxT + kTile - 1) / kTile;
+    const int nc = (maxT + kChunk - 1) / kChunk;
+    const int c0 = (int)((long long)nc * split / a.splits), c1 = (int)((long long)nc * (split + 1) / a.splits);
 
-    // copy the raw K/V (+ scale) rows of tile t into stage t % kXStages; every
-    // thread commits one group per call (empty beyond the last tile)
-    auto issue = [&](int t) {
-      if (t < ntiles) {
-        const uint32_t st = sraw_base + (uint32_t)((t % kXStages) * Tr::kStageBytes);
-        const int tt0 = t * kTile;
-        const int page = __ldg(prow + tt0 / a.P);  // one page holds the whole tile
-        const bool pok = page >= 0 && page < a.num_pages;
-        if (!pok) pass_bad = 1;
-        const long long row0 = ((long long)(pok ? page : 0) * a.H + h) * a.P + tt0 % a.P;
-        constexpr int kChunks = Tr::kRow / 16;  // 16-byte pieces of one row
-        for (int i = tid; i < Tr::kCopies; i += kXThreads) {
-          if (i < 2 * kTile * kChunks) {
-            const int kv = i / (kTile * kChunks), j = i % (kTile * kChunks);
-            const int tok = j / kChunks, ch = j % kChunks;
-            const bool valid = pok && tt0 + tok < maxT;
-            const uint8_t* src = (kv ? a.vd : a.kd) + (row0 + tok) * Tr::kRow + ch * 16;
-            cp_async16(st + (uint32_t)(kv * kTile * Tr::kRow + tok * Tr::kRow + ch * 16),
-                       valid ? src : a.kd, valid);
+    // issue the raw copies of chunk c into ring stage st (warp 0); chunks go
+    // through the two stages in order, so chunk number k (counted over the
+    // CTA's life) uses stage k & 1 with mbarrier phase parity (k >> 1) & 1
+    auto issue = [&](int c, uint32_t st) {
+      const uint32_t bar = bar_raw0 + 8 * st;
+      const uint32_t dst0 = sm_u32 + kSRaw + st * Tr::kStage;
+      const int t = lane >> 2, kind = lane & 3;  // lanes 0..15: tile t, tensor kind
+      bool mine = false;
+      uint32_t bytes = 0;
+      const uint8_t* src = nullptr;
+      uint32_t dst = 0;
+      bool bad = false;
+      if (lane < 16 && (kind < 2 || Tr::kScales)) {
+        const int tok0 = c * kChunk + 16 * t;
+        if (tok0 < maxT) {
+          const int page = __ldg(prow + tok0 / a.P);
+          if (page >= 0 && page < a.num_pages) {
+            const long long rowi = ((long long)page * a.H + h) * a.P + tok0 % a.P;
+            const int rb = kind < 2 ? Tr::kRow : 8;
+            const uint8_t* pool = kind == 0 ? a.kd : kind == 1 ? a.vd : kind == 2 ? a.ks : a.vs;
+            src = pool + rowi * rb;
+            bytes = 16u * rb;
+            dst = dst0 + (kind == 0 ? 0 : kind == 1 ? Tr::kData : kind == 2 ? 2 * Tr::kData
+                                                                             : 2 * Tr::kData + Tr::kScl) +
+                  t * 16 * rb;
+            mine = true;
           } else {
-            const int j = i - 2 * kTile * kChunks, kv = j / kTile, tok = j % kTile;
-            const bool valid = pok && tt0 + tok < maxT;
-            const uint8_t* src = (kv ? a.vs : a.ks) + (row0 + tok) * 8;
-            cp_async8(st + (uint32_t)(2 * kTile * Tr::kRow + kv * kTile * 8 + tok * 8),
-                      valid ? src : a.kd, valid);
+            bad = true;
           }
         }
       }
-      cp_async_commit();
+      const uint32_t okmask = __ballot_sync(0xffffffffu, mine && kind == 0);
+      uint32_t total = bytes;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) pass_bad = 1;
+      if (lane == 0) {
+        uint32_t tiles = 0;
+        for (int tt = 0; tt < 4; ++tt) tiles |= ((okmask >> (4 * tt)) & 1u) << tt;
+        stage_ok[st] = tiles;
+        mbar_arrive_tx(bar, total);
+      }
+      __syncwarp();
+      if (mine) bulk_g2s(dst, src, bytes, bar);
     };
-#pragma unroll 1
-    for (int t = 0; t < kXStages - 1; ++t) issue(t);
 
-    for (int t = 0; t < ntiles; ++t) {
-      issue(t + kXStages - 1);
-      cp_async_wait<kXStages - 1>();  // this thread's copies of tile t have landed
-      __syncthreads();                // ... and every other thread's
-      // dequantize tile t (absent tokens and bad pages were zero-filled)
+    float m = -INFINITY, l = 0.f;
+    bool first = true;
+    for (int c = c0; c < min(c0 + 2, c1); ++c) {
+      if (warp == 0) issue(c, n_raw_issued & 1u);
+      ++n_raw_issued;
+    }
+    for (int c = c0; c < c1; ++c) {
+      // ---- raw chunk c landed ----
+      const uint32_t st = n_raw_used & 1u;
+      const bool ok = mbar_wait_bounded(bar_raw0 + 8 * st, (n_raw_used >> 1) & 1u);
+      ++n_raw_used;
+      if (!ok) dead = 1;
+      // ---- dequantize chunk c into the swizzled bf16 K and V tiles ----
       {
-        const uint8_t* stage = &sraw[t % kXStages][0];
-        uint32_t ok_[8], ov_[8];
-        dequant_block<F>(raw_block<F>(stage, 0, my_tok, my_blk), ok_);
-        dequant_block<F>(raw_block<F>(stage, 1, my_tok, my_blk), ov_);
-        uint8_t* kdst = &sm[0][my_tok * kXStride + my_blk * 32];
-        uint8_t* vdst = &sm[1][my_tok * kXStride + my_blk * 32];
-        reinterpret_cast<uint4*>(kdst)[0] = make_uint4(ok_[0], ok_[1], ok_[2], ok_[3]);
-        reinterpret_cast<uint4*>(kdst)[1] = make_uint4(ok_[4], ok_[5], ok_[6], ok_[7]);
-        reinterpret_cast<uint4*>(vdst)[0] = make_uint4(ov_[0], ov_[1], ov_[2], ov_[3]);
-        reinterpret_cast<uint4*>(vdst)[1] = make_uint4(ov_[4], ov_[5], ov_[6], ov_[7]);
+        const uint8_t* stage = sm + kSRaw + st * Tr::kStage;
+        const int tt = tid >> 1, hf = tid & 1;
+        const bool tok_ok = ((stage_ok[st] >> (tt >> 4)) & 1u) && c * kChunk + tt < maxT;
+        uint32_t kw[32], vw[32];
+        if (tok_ok) {
+          dequant_half<F>(stage, stage + 2 * Tr::kData, tt, hf, kw);
+          dequant_half<F>(stage + Tr::kData, stage + 2 * Tr::kData + Tr::kScl, tt, hf, vw);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) kw[i] = vw[i] = 0u;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint32_t off = hf * (kChunk * 128) + sw_off(tt, cc);
+          *reinterpret_cast<uint4*>(sm + kSK + off) = make_uint4(kw[4 * cc], kw[4 * cc + 1], kw[4 * cc + 2], kw[4 * cc + 3]);
+          *reinterpret_cast<uint4*>(sm + kSV + off) = make_uint4(vw[4 * cc], vw[4 * cc + 1], vw[4 * cc + 2], vw[4 * cc + 3]);
+        }
       }
+      fence_proxy_async();
+      tc_fence_before();
       __syncthreads();
-      if (!__any_sync(0xffffffffu, act[0] || act[1])) continue;  // no row of this warp in the pass
-
-      const uint32_t kbase = sbase;
-      const uint32_t vbase = sbase + (uint32_t)kXTile;
-      // ---- S = Q K^T (16 rows x 16 tokens) ----
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      tc_fence_after();
+      if (dead) break;
+      // ---- refill the consumed stage with chunk c + 2 ----
+      if (c + 2 < c1) {
+        if (warp == 0) {
+          fence_proxy_async();
+          issue(c + 2, n_raw_issued & 1u);
+        }
+        ++n_raw_issued;
+      }
+      // ---- S = Q K^T ----
+      if (tid == 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint64_t ad = sw128_desc(sm_u32 + kSQ + (j >> 2) * (kXRows * 128) + (j & 3) * 32, 1024);
+          const uint64_t bd = sw128_desc(sm_u32 + kSK + (j >> 2) * (kChunk * 128) + (j & 3) * 32, 1024);
+          mma_ss(tmem + kColS, ad, bd, kIdQK, j > 0);
+        }
+        mma_commit(bar_s);
+      }
+      const bool sok = mbar_wait_bounded(bar_s, n_s & 1u);
+      ++n_s;
+      tc_fence_after();
+      if (!__all_sync(0xffffffffu, sok)) {
+        if (lane == 0) dead = 1;
+      }
+      // ---- online softmax of this thread's row ----
+      uint32_t sv[64];
       {
-        const int mi = lane >> 3, rr = lane & 7;
-        const uint32_t lrow = (uint32_t)((rr + 8 * (mi >> 1)) * kXStride + (mi & 1) * 16);
+        uint32_t t0[32], t1[32];
+        tmem_ld32(tmem + lane_off + kColS, t0);
+        tmem_ld32(tmem + lane_off + kColS + 32, t1);
+        tmem_wait_ld();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t b00, b01, b10, b11;
-          ldsm_x4(kbase + lrow + ks * 32, b00, b01, b10, b11);
-          mma16816<BF>(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
-          mma16816<BF>(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
+        for (int j = 0; j < 32; ++j) {
+          sv[j] = t0[j];
+          sv[32 + j] = t1[j];
         }
       }
-      // ---- online softmax (base 2) per row; masked tokens and inactive rows: -inf ----
-      float x[2][4];  // [n-tile][c0 c1 (row r4), c2 c3 (row r4 + 8)]
+      float mx = -INFINITY;
+      if (act && (c + 1) * kChunk <= Tr_) {  // every token of the chunk is in this row's prefix
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = e >> 1;
-          const int tok = t * kTile + nt * 8 + 2 * c + (e & 1);
-          x[nt][e] = (act[i] && tok < Tr_[i]) ? sacc[nt][e] * cs[i] : -INFINITY;
+        for (int j = 0; j < 64; ++j) {
+          const float x = __uint_as_float(sv[j]) * cs;
+          sv[j] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
         }
-      float mx[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        mx[i] = fmaxf(fmaxf(x[0][2 * i], x[0][2 * i + 1]), fmaxf(x[1][2 * i], x[1][2 * i + 1]));
-        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-      }
-      const bool grow0 = mx[0] > m[0] + 8.f, grow1 = mx[1] > m[1] + 8.f;
-      if (__any_sync(0xffffffffu, grow0 || grow1)) {
-        const float n0 = grow0 ? mx[0] : m[0], n1 = grow1 ? mx[1] : m[1];
-        const float al0 = grow0 ? ex2x(m[0] - n0) : 1.f, al1 = grow1 ? ex2x(m[1] - n1) : 1.f;
-        l[0] *= al0;
-        l[1] *= al1;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          o[j][0] *= al0;
-          o[j][1] *= al0;
-          o[j][2] *= al1;
-          o[j][3] *= al1;
-        }
-        m[0] = n0;
-        m[1] = n1;
-      }
-      float p[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = e >> 1;
-          p[nt][e] = (x[nt][e] == -INFINITY) ? 0.f : ex2x(x[nt][e] - m[i]);
-          l[i] += p[nt][e];
-        }
-      // ---- O += P V: P from the S accumulators (A operand), V by ldmatrix.trans ----
-      uint32_t pa[4], pl[4];
-      if (BF) {
-        pa[0] = pack_bf2(p[0][0], p[0][1]);
-        pa[1] = pack_bf2(p[0][2], p[0][3]);
-        pa[2] = pack_bf2(p[1][0], p[1][1]);
-        pa[3] = pack_bf2(p[1][2], p[1][3]);
-        pl[0] = pack_bf2(p[0][0] - bf16_bits_to_float(pa[0] & 0xFFFF), p[0][1] - bf16_bits_to_float(pa[0] >> 16));
-        pl[1] = pack_bf2(p[0][2] - bf16_bits_to_float(pa[1] & 0xFFFF), p[0][3] - bf16_bits_to_float(pa[1] >> 16));
-        pl[2] = pack_bf2(p[1][0] - bf16_bits_to_float(pa[2] & 0xFFFF), p[1][1] - bf16_bits_to_float(pa[2] >> 16));
-        pl[3] = pack_bf2(p[1][2] - bf16_bits_to_float(pa[3] & 0xFFFF), p[1][3] - bf16_bits_to_float(pa[3] >> 16));
       } else {
-        pa[0] = pack_h2(p[0][0], p[0][1]);
-        pa[1] = pack_h2(p[0][2], p[0][3]);
-        pa[2] = pack_h2(p[1][0], p[1][1]);
-        pa[3] = pack_h2(p[1][2], p[1][3]);
-        pl[0] = pl[1] = pl[2] = pl[3] = 0u;
-      }
-      {
-        const int mi = lane >> 3, rr = lane & 7;
-        const uint32_t lrow = (uint32_t)((rr + 8 * (mi & 1)) * kXStride + (mi >> 1) * 16);
 #pragma unroll
-        for (int j2 = 0; j2 < 8; ++j2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vbase + lrow + j2 * 32, b0, b1, b2, b3);
-          mma16816<BF>(o[2 * j2], pa[0], pa[1], pa[2], pa[3], b0, b1);
-          mma16816<BF>(o[2 * j2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
-          if (BF) {
-            mma16816<BF>(o[2 * j2], pl[0], pl[1], pl[2], pl[3], b0, b1);
-            mma16816<BF>(o[2 * j2 + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+        for (int j = 0; j < 64; ++j) {
+          const int tok = c * kChunk + j;
+          const float x = (act && tok < Tr_) ? __uint_as_float(sv[j]) * cs : -INFINITY;
+          sv[j] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      }
+      const bool grow = mx > m + 8.f;
+      const float m_new = grow ? mx : m;
+      // rescale what O already holds (warp-uniform tensor-memory access)
+      if (__any_sync(0xffffffffu, grow && m != -INFINITY && !first)) {
+        const float al = (grow && m != -INFINITY) ? ex2x(m - m_new) : 1.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_off + kColO + 32 * q4, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * al);
+          tmem_st32(tmem + lane_off + kColO + 32 * q4, ov);
+        }
+        l *= al;
+      } else if (grow && m != -INFINITY) {
+        l *= ex2x(m - m_new);
+      }
+      m = m_new;
+      if constexpr (Tr::kF16) {
+        // P <= 2^8 in f16 (relative rounding 2^-11)
+        uint32_t ph[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x0 = __uint_as_float(sv[2 * j]), x1 = __uint_as_float(sv[2 * j + 1]);
+          const float p0 = (x0 == -INFINITY) ? 0.f : ex2x(x0 - m);
+          const float p1 = (x1 == -INFINITY) ? 0.f : ex2x(x1 - m);
+          l += p0 + p1;
+          uint32_t r;
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));
+          ph[j] = r;
+        }
+        tmem_st32(tmem + lane_off + kColPh, ph);
+        tmem_wait_st();
+      } else {
+        uint32_t ph[32], pl[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x0 = __uint_as_float(sv[2 * j]), x1 = __uint_as_float(sv[2 * j + 1]);
+          const float p0 = (x0 == -INFINITY) ? 0.f : ex2x(x0 - m);
+          const float p1 = (x1 == -INFINITY) ? 0.f : ex2x(x1 - m);
+          l += p0 + p1;
+          ph[j] = bf2(p0, p1);
+          const float r0 = p0 - bf16_bits_to_float(ph[j] & 0xFFFFu);
+          const float r1 = p1 - bf16_bits_to_float(ph[j] >> 16);
+          pl[j] = bf2(r0, r1);
+        }
+        tmem_st32(tmem + lane_off + kColPh, ph);
+        tmem_st32(tmem + lane_off + kColPl, pl);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (dead) break;
+      // ---- O += P V (two 64-column halves of head_dim; P high and low parts) ----
+      if (tid == 0) {
+#pragma unroll
+        for (int j = 0; j < kChunk / 16; ++j) {
+#pragma unroll
+          for (int nh = 0; nh < 2; ++nh) {
+            const uint64_t bd = sw128_desc(sm_u32 + kSV + nh * (kChunk * 128) + j * 2048, 1024);
+            const uint32_t d = tmem + kColO + 64 * nh;
+            mma_ts(d, tmem + kColPh + 8 * j, bd, kIdPV, (first && j == 0) ? 0u : 1u);
+            if (!Tr::kF16) mma_ts(d, tmem + kColPl + 8 * j, bd, kIdPV, 1u);
+          }
+        }
+        mma_commit(bar_o);
+      }
+      const bool ook = mbar_wait_bounded(bar_o, n_o & 1u);
+      ++n_o;
+      tc_fence_after();
+      if (!__all_sync(0xffffffffu, ook)) {
+        if (lane == 0) dead = 1;
+      }
+      first = false;
+    }
+    __syncthreads();
+    // ---- this pass's rows: partial (or final) output of this split ----
+    const bool poison = pass_bad != 0 || dead != 0;
+    if (pass_bad && tid == 0) atomicOr(a.err, kErrRange);
+    if (dead && tid == 0) atomicOr(a.err, kErrTimeout);
+    {
+      const bool has = !first && l > 0.f;
+      const float inv = (has && !poison) ? vf / l : 0.f;
+      const long long rowg = qi * a.Hq + qhead;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t ov[32];
+        if (!first) {  // warp-uniform: every thread of the pass has run the chunks
+          tmem_ld32(tmem + lane_off + kColO + 32 * q4, ov);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = 0u;
+        }
+        if (act && qvalid) {
+          if (a.splits == 1) {
+            uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + rowg * kHeadDim + 32 * q4);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              dst[j] = bf16_rne_bits(__uint_as_float(ov[2 * j]) * inv) |
+                       (bf16_rne_bits(__uint_as_float(ov[2 * j + 1]) * inv) << 16);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(a.part_o + (rowg * a.splits + split) * kHeadDim + 32 * q4);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
+                                   __uint_as_float(ov[4 * j + 2]) * inv, __uint_as_float(ov[4 * j + 3]) * inv);
           }
         }
       }
+      if (act && qvalid && a.splits > 1)
+        a.part_lse[rowg * a.splits + split] = poison ? INFINITY : (has ? m + __log2f(l) : -INFINITY);
+      if (act) row_done = true;
     }
-    cp_async_wait<0>();  // only empty groups remain; the stages are free
-    __syncthreads();     // pass_bad complete; buffers free for the next pass
-    if (pass_bad) {
-      if (tid == 0) atomicOr(a.err, kErrRange);
-      poison[0] = poison[0] || act[0];
-      poison[1] = poison[1] || act[1];
-    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     if (tid == 0)
       for (int rho = 0; rho < kXRows; ++rho)
         if (row_seq[rho] == s) row_seq[rho] = -1;
     __syncthreads();
   }
+  // rows that never ran (invalid, or left after a wait ran out): zero output
+  if (qvalid && !row_done) {
+    const long long rowg = qi * a.Hq + qhead;
+    if (a.splits == 1) {
+      uint4* dst = reinterpret_cast<uint4*>(a.out + rowg * kHeadDim);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) dst[j] = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      a.part_lse[rowg * a.splits + split] = dead ? INFINITY : -INFINITY;
+    }
+  }
+  // copies and MMAs still in flight (after a wait ran out): give them a
+  // bounded chance to complete before the CTA frees its tensor memory and exits
+  if (dead) {
+    for (uint32_t t = n_raw_used; t < n_raw_issued; ++t) mbar_wait_bounded(bar_raw0 + 8 * (t & 1u), (t >> 1) & 1u);
+    if (n_s > 0) mbar_wait_bounded(bar_s, (n_s - 1) & 1u);
+    if (n_o > 0) mbar_wait_bounded(bar_o, (n_o - 1) & 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols) : "memory");
+}
 
-  // ---- normalize and write: row i holds d = 8 j + 2c, +1 -------------------------
+// out[row] = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M) over the splits;
+// +inf (poisoned) gives zeros, all -inf (no tokens) gives zeros.  One warp per
+// row, lanes own four head_dim elements.
+__global__ void __launch_bounds__(256) extend_merge_kernel(ExtendArgs a, long long rows) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float lse = lane < a.splits ? a.part_lse[row * a.splits + lane] : -INFINITY;
+  float M = lse;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    l[i] += __shfl_xor_sync(0xffffffffu, l[i], 1);
-    l[i] += __shfl_xor_sync(0xffffffffu, l[i], 2);
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  uint2 ov = make_uint2(0u, 0u);
+  if (M != INFINITY && M != -INFINITY) {
+    const float w = (lse == -INFINITY) ? 0.f : ex2x(lse - M);
+    float den = w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < a.splits; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      if (ws == 0.f) continue;
+      const float4 v = *reinterpret_cast<const float4*>(a.part_o + (row * a.splits + s) * kHeadDim + lane * 4);
+      acc.x += ws * v.x;
+      acc.y += ws * v.y;
+      acc.z += ws * v.z;
+      acc.w += ws * v.w;
+    }
+    const float inv = 1.f / den;
+    ov.x = bf16_rne_bits(acc.x * inv) | (bf16_rne_bits(acc.y * inv) << 16);
+    ov.y = bf16_rne_bits(acc.z * inv) | (bf16_rne_bits(acc.w * inv) << 16);
   }
-  const float vf = a.vfac ? __ldg(a.vfac + h) : a.v_factor;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    if (!qvalid[i]) continue;
-    const float inv = (poison[i] || !(l[i] > 0.f)) ? 0.f : vf / l[i];
-    uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + (qrow[i] * a.Hq + qhead[i]) * kHeadDim);
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      dst[4 * j + c] = bf16_rne_bits(o[j][2 * i] * inv) | (bf16_rne_bits(o[j][2 * i + 1] * inv) << 16);
-  }
+  *reinterpret_cast<uint2*>(a.out + row * kHeadDim + lane * 4) = ov;
 }
 
 template <kvq_format F>
 cudaError_t launch_extend_as(const ExtendArgs& a, cudaStream_t stream) {
+  static_assert(XTraits<F>::kSmem <= 227 * 1024, "extend tiles exceed shared memory");
+  cudaError_t e = cudaFuncSetAttribute(extend_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       XTraits<F>::kSmem);
+  if (e != cudaSuccess) return e;
   const long long rows = (long long)a.n * a.G;
-  dim3 grid((unsigned)((rows + kXRows - 1) / kXRows), (unsigned)a.H);
-  extend_kernel<F><<<grid, kXThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  dim3 grid((unsigned)((rows + kXRows - 1) / kXRows), (unsigned)a.H, (unsigned)a.splits);
+  extend_kernel<F><<<grid, kXThreads, XTraits<F>::kSmem, stream>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.splits > 1) {
+    const long long orows = (long long)a.n * a.Hq;
+    extend_merge_kernel<<<(unsigned)((orows + 7) / 8), 256, 0, stream>>>(a, orows);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace
+
+int extend_splits(const Geometry& g, int num_q_tokens, int num_q_heads, int max_pages_per_seq,
+                  int device) {
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  const int G = num_q_heads / g.kv_heads;
+  const long long ctas = (((long long)num_q_tokens * G + kXRows - 1) / kXRows) * g.kv_heads;
+  const long long chunks = ((long long)max_pages_per_seq * g.page_size + kChunk - 1) / kChunk;
+  // about four CTAs per SM over the grid, at least four chunks per split
+  long long s = ctas > 0 ? (4LL * sms + ctas - 1) / ctas : 1;
+  s = std::min<long long>(s, std::max<long long>(1, chunks / 4));
+  return (int)std::max<long long>(1, std::min<long long>(s, kMaxSplits));
+}
+
+size_t extend_workspace_bytes(int splits, int num_q_tokens, int num_q_heads) {
+  if (splits <= 1) return 0;
+  const size_t rows = (size_t)num_q_tokens * num_q_heads;
+  return ((rows * splits * kHeadDim * sizeof(float) + 255) & ~(size_t)255) +
+         ((rows * splits * sizeof(float) + 255) & ~(size_t)255);
+}
 
 cudaError_t launch_extend(const Geometry& g, const LayerView& L, const void* q, int num_q_heads,
                           int num_q_tokens, const int32_t* q_seq, const int32_t* q_len,
                           const int32_t* page_table, int num_seqs, int max_pages_per_seq,
                           float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
-                          void* out, int* err, cudaStream_t stream) {
+                          void* out, int* err, int splits, void* workspace, cudaStream_t stream) {
   ExtendArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.out = static_cast<uint16_t*>(out);
@@ -533,6 +769,13 @@ cudaError_t launch_extend(const Geometry& g, const LayerView& L, const void* q, 
   a.qscale = sm_scale * 1.4426950408889634f * (a.kfac ? 1.0f : k_factor);
   a.v_factor = v_factor;
   a.err = err;
+  a.splits = std::max(1, splits);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t rows = (size_t)num_q_tokens * num_q_heads;
+  a.part_o = reinterpret_cast<float*>(ws);
+  a.part_lse = ws ? reinterpret_cast<float*>(ws + ((rows * a.splits * kHeadDim * sizeof(float) + 255) &
+                                                   ~(size_t)255))
+                  : nullptr;
   if (num_q_tokens == 0) return cudaSuccess;
   switch (g.fmt) {
     case KVQ_BF16: return launch_extend_as<KVQ_BF16>(a, stream);

@@ -75,13 +75,18 @@ cudaError_t launch_calibrate(const Geometry& g, const void* k, const void* v, in
                              unsigned* amax_scratch, float* scale, float* recip,
                              cudaStream_t stream);
 
-// Extend attention (kvq_extend.cu): one pass over each sequence's K/V tiles per
-// 64 (query, q head) rows of a kv head; no workspace.
+// Extend attention (kvq_extend.cu): per 128 (query, q head) rows of a kv head
+// and per split of each sequence's context, one pass over its K/V chunks on
+// the tcgen05 tensor cores; with splits > 1 the workspace holds the partial
+// outputs (extend_workspace_bytes) and a merge kernel combines them.
+int extend_splits(const Geometry& g, int num_q_tokens, int num_q_heads, int max_pages_per_seq,
+                  int device);
+size_t extend_workspace_bytes(int splits, int num_q_tokens, int num_q_heads);
 cudaError_t launch_extend(const Geometry& g, const LayerView& L, const void* q, int num_q_heads,
                           int num_q_tokens, const int32_t* q_seq, const int32_t* q_len,
                           const int32_t* page_table, int num_seqs, int max_pages_per_seq,
                           float sm_scale, float k_factor, float v_factor, const HeadScales& hs,
-                          void* out, int* err, cudaStream_t stream);
+                          void* out, int* err, int splits, void* workspace, cudaStream_t stream);
 
 // Decode attention plan: how many warp workers and how much workspace.
 struct DecodePlan {

@@ -17,15 +17,15 @@ constexpr int kMergeMaxWarps = 32;
 
 // One CTA per (unit, q head of the unit's group); its warps split the unit's
 // partials (warp i takes partials i, i + nwarps, ...), each lane owning four
-// head_dim elements, and reduce in shared memory.  The warp count is chosen on
-// the host from the average number of partials per unit, so a unit split over
-// hundreds of workers (small batches) is merged by up to 32 warps.
+// head_dim elements, in one pass (every load of a batch in flight together),
+// and combine in shared memory.  The warp count is chosen on the host from the
+// average number of partials per unit, so a unit split over hundreds of
+// workers (small batches) is merged by up to 32 warps.
 __global__ void __launch_bounds__(kMergeMaxWarps * 32) merge_kernel(DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float4 s_acc[kMergeMaxWarps][32];
   __shared__ float s_den[kMergeMaxWarps];
   __shared__ float s_max[kMergeMaxWarps];
-  __shared__ int s_poison;
   const long long u = blockIdx.x / kGroupMax;
   const int g = (int)(blockIdx.x - u * kGroupMax);
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5, nwarps = blockDim.x >> 5;
@@ -52,76 +52,73 @@ __global__ void __launch_bounds__(kMergeMaxWarps * 32) merge_kernel(DecodeArgs a
     return dense || worker_start(total, w, nw) != worker_start(total, w + 1, nw);
   };
 
-  // ---- M = max lse over the unit's partials; +inf marks a poisoned partial ----
-  float M = -INFINITY;
-  bool poison = false;
-  for (int w = wf + tid; w <= wl; w += blockDim.x) {
-    if (!nonempty(w)) continue;
-    const float lse = a.part_lse[(u + w) * kGroupMax + g];
-    poison |= (lse == INFINITY);
-    M = fmaxf(M, lse);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  poison = __any_sync(0xffffffffu, poison);
-  if (tid == 0) s_poison = 0;
-  __syncthreads();
-  if (lane == 0) {
-    s_max[wi] = M;
-    if (poison) s_poison = 1;
-  }
-  __syncthreads();
-  for (int i = 0; i < nwarps; ++i) M = fmaxf(M, s_max[i]);
-  if (s_poison) {
-    if (wi == 0) *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
-    return;
-  }
-
-  // ---- this warp's share: sum_w 2^(lse_w - M) o_w and the weights ----
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
+  // ---- one pass: warp wi takes partials wf + wi + k * nwarps, loading each
+  // lse with its output slice, and keeps (max, weighted sum, weight) relative
+  // to its own running maximum; +inf marks a poisoned partial ----
   const float* base = a.part_o + (u * kGroupMax + g) * kHeadDim + lane * 4;
   const long long pstride = (long long)kGroupMax * kHeadDim;  // floats between slots
-  int w = wf + wi;
-  // two partials per step: both loads in flight together
-  for (; w + nwarps <= wl; w += 2 * nwarps) {
-    const int w2 = w + nwarps;
-    const bool e1 = nonempty(w), e2 = nonempty(w2);
-    const float l1 = e1 ? a.part_lse[(u + w) * kGroupMax + g] : -INFINITY;
-    const float l2 = e2 ? a.part_lse[(u + w2) * kGroupMax + g] : -INFINITY;
-    const float4 v1 = e1 ? *reinterpret_cast<const float4*>(base + (long long)w * pstride)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 v2 = e2 ? *reinterpret_cast<const float4*>(base + (long long)w2 * pstride)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float t1 = e1 ? ex2(l1 - M) : 0.f, t2 = e2 ? ex2(l2 - M) : 0.f;
-    den += t1 + t2;
-    acc.x += t1 * v1.x + t2 * v2.x;
-    acc.y += t1 * v1.y + t2 * v2.y;
-    acc.z += t1 * v1.z + t2 * v2.z;
-    acc.w += t1 * v1.w + t2 * v2.w;
-  }
-  if (w <= wl && nonempty(w)) {
-    const float t1 = ex2(a.part_lse[(u + w) * kGroupMax + g] - M);
-    const float4 v1 = *reinterpret_cast<const float4*>(base + (long long)w * pstride);
-    den += t1;
-    acc.x += t1 * v1.x;
-    acc.y += t1 * v1.y;
-    acc.z += t1 * v1.z;
-    acc.w += t1 * v1.w;
+  float m = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool poison = false;
+  for (int w = wf + wi; w <= wl; w += 4 * nwarps) {
+    float l[4];
+    float4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int wi2 = w + i * nwarps;
+      const bool e = wi2 <= wl && nonempty(wi2);
+      l[i] = e ? a.part_lse[(u + wi2) * kGroupMax + g] : -INFINITY;
+      v[i] = e ? *reinterpret_cast<const float4*>(base + (long long)wi2 * pstride)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float mb = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+    poison |= (mb == INFINITY);
+    if (mb > m) {  // rescale what this warp has so far
+      const float f = (m == -INFINITY) ? 0.f : ex2(m - mb);
+      den *= f;
+      acc.x *= f;
+      acc.y *= f;
+      acc.z *= f;
+      acc.w *= f;
+      m = mb;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float t = (l[i] == -INFINITY || m == INFINITY) ? 0.f : ex2(l[i] - m);
+      den += t;
+      acc.x += t * v[i].x;
+      acc.y += t * v[i].y;
+      acc.z += t * v[i].z;
+      acc.w += t * v[i].w;
+    }
   }
   if (nwarps > 1) {
     s_acc[wi][lane] = acc;
-    if (lane == 0) s_den[wi] = den;
+    if (lane == 0) {
+      s_den[wi] = den;
+      s_max[wi] = poison ? INFINITY : m;
+    }
     __syncthreads();
     if (wi != 0) return;
-    for (int i = 1; i < nwarps; ++i) {
-      const float4 v = s_acc[i][lane];
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-      den += s_den[i];
+    float M = -INFINITY;
+    for (int i = 0; i < nwarps; ++i) M = fmaxf(M, s_max[i]);
+    poison = (M == INFINITY);
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    den = 0.f;
+    for (int i = 0; i < nwarps; ++i) {
+      const float mi = s_max[i];
+      const float f = (mi == -INFINITY || poison) ? 0.f : ex2(mi - M);
+      const float4 x = s_acc[i][lane];
+      den += f * s_den[i];
+      acc.x += f * x.x;
+      acc.y += f * x.y;
+      acc.z += f * x.z;
+      acc.w += f * x.w;
     }
+  }
+  if (poison) {
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+    return;
   }
   const float inv = 1.f / den;
   uint2 ov;
@@ -133,7 +130,8 @@ __global__ void __launch_bounds__(kMergeMaxWarps * 32) merge_kernel(DecodeArgs a
 }  // namespace
 
 cudaError_t launch_merge(const DecodeArgs& a, int64_t num_units, cudaStream_t stream) {
-  // about four partials per warp on average, 1 to 32 warps per CTA
+  // about four partials per warp on average (one batch of loads), 1 to 32
+  // warps per CTA
   const int64_t per_unit = (a.num_workers + num_units - 1) / num_units + 1;
   int warps = 1;
   while (warps < kMergeMaxWarps && warps * 4 < per_unit) warps <<= 1;

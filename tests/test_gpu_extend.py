@@ -104,3 +104,29 @@ def test_extend_bad_rows_and_lengths(kvq, cuda):
     got = _gpu_extend(c, wl, q, np.array([0, 1, 1, 0], np.int32), q_len)
     assert c.device_error() == kvq._binding._STATUS_CODES["KVQ_ERR_DEVICE_RANGE"]
     assert (got[1] == 0).all() and (got[3] != 0).any()
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "nvfp4"])
+def test_extend_split_and_unsplit_plans_agree(kvq, orc, cuda, fmt):
+    """Long contexts: the fastest plan splits each sequence's context across
+    CTAs (partials merged from the workspace); without a workspace the call
+    runs unsplit.  Both match the oracle."""
+    wl = synth.make_workload(f"exs_{fmt}", fmt, Hq=64, Hkv=8, seq_lens=[3000, 1200, 4100], seed=8)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    q, q_seq, q_len = _queries(wl, [16, 5, 16], seed=4)
+    need = kvq.kvq_extend_workspace_size(c.handle, len(q_seq), wl.Hq, wl.max_pages)
+    assert need > 0
+    ref, rc = oracle_cache_for(orc, wl).extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
+    assert rc == 0
+    outs = []
+    for ws_bytes in (need, 16):
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        out = c.extend_attention(0, bits_to_cuda(q), torch.from_numpy(q_seq).cuda(),
+                                 torch.from_numpy(q_len).cuda(), torch.from_numpy(wl.page_table).cuda(),
+                                 wl.sm_scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert c.device_error() == 0
+        got = synth.bf16_bits_to_float(cuda_to_bits(out)).astype(np.float64)
+        assert_attention_close(got, ref, f"{fmt} extend workspace {ws_bytes}")
+        outs.append(got)
