@@ -13,9 +13,9 @@
 // heads per kv head) -- one row per thread and per tensor-memory lane -- and
 // one split of the context (gridDim.z splits; their partial outputs and
 // log-sum-exps are merged by extend_merge_kernel).  Per 64-token chunk:
-//   - lanes of warp 0 bulk-copy the raw K/V rows (and block scales) of the
-//     chunk's four 16-token (page, kv head) slabs into a two-stage ring,
-//     completing on an mbarrier;
+//   - the dequant warps copy the raw K/V rows (and block scales) of the
+//     chunk into a ring of raw stages several chunks ahead with cp.async,
+//     each thread its own slice, completing on the stage's mbarrier;
 //   - every thread dequantizes half a token row of K and of V into f16 (FP8,
 //     NVFP4) or bf16 (bf16, FP4 block-16) tiles in the 128-byte-swizzled
 //     layout the tensor cores read (exact for every format: the per-tensor /
@@ -44,23 +44,24 @@ namespace kvq {
 namespace {
 
 constexpr int kXRows = 128;        // (query, q head) rows per CTA = TMEM lanes
-constexpr int kXThreads = 128;
+constexpr int kXThreads = 288;     // warps 0-3: rows; 4-7: dequant; 8: copies and MMA issue
+constexpr int kSlots = 3;          // raw stages, K/V tiles and S slots in flight
 constexpr int kChunk = 64;         // tokens per chunk (four 16-token tiles)
 constexpr int kMaxSplits = 16;
 constexpr uint32_t kXWaitLimit = 1u << 22;
 
-// tensor-memory columns
-constexpr uint32_t kColS = 0;      // S: 64 fp32 columns
-constexpr uint32_t kColO = 64;     // O: 128 fp32 columns (two halves of head_dim)
-constexpr uint32_t kColPh = 192;   // P high bf16 part: 32 columns (bf16x2)
-constexpr uint32_t kColPl = 224;   // P low part
-constexpr uint32_t kTmemCols = 256;
+// tensor-memory columns: three S slots (64 fp32 columns each; P of a chunk
+// is written back over its own S slot: f16 in 32 columns, or bf16 high and
+// low parts in 64) and O (128 fp32 columns, two halves of head_dim)
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 64 * kSlots;
+constexpr uint32_t kTmemCols = 512;
 
 // shared memory (dynamic, 1024-byte aligned offsets)
-constexpr int kSQ = 0;                        // Q: 2 K-atoms x 128 rows x 128 B
-constexpr int kSK = kSQ + 2 * kXRows * 128;   // K: 2 atoms x 64 tokens x 128 B
-constexpr int kSV = kSK + 2 * kChunk * 128;   // V: same layout, read MN-major
-constexpr int kSRaw = kSV + 2 * kChunk * 128; // raw stages
+constexpr int kSQ = 0;                              // Q: 2 K-atoms x 128 rows x 128 B
+constexpr int kSKV = kSQ + 2 * kXRows * 128;        // slots of [K tile | V tile]
+constexpr int kTileKV = 2 * kChunk * 128;           // one K (or V) tile: 2 atoms x 64 tokens x 128 B
+constexpr int kSRaw = kSKV + kSlots * 2 * kTileKV;  // raw stages
 
 template <kvq_format F>
 struct XTraits {
@@ -74,7 +75,9 @@ struct XTraits {
   static constexpr int kData = kChunk * kRow;
   static constexpr int kScl = kScales ? kChunk * 8 : 0;
   static constexpr int kStage = 2 * kData + 2 * kScl;
-  static constexpr int kSmem = kSRaw + 2 * kStage + 1024;  // + alignment slack
+  // raw stages in flight: as many as shared memory leaves room for
+  static constexpr int kRaw = (F == KVQ_BF16) ? 3 : (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) ? 4 : 6;
+  static constexpr int kSmem = kSRaw + kRaw * kStage + 1024;  // + alignment slack
 };
 
 struct ExtendArgs {
@@ -104,9 +107,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)_
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -120,10 +120,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   while (!ok && ++polls < kXWaitLimit) ok = mbar_try_wait(bar, parity);
   return ok;
 }
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar) : "memory");
+// Asynchronous global -> shared copy of `bytes` (16 or 4) that reads
+// `valid ? bytes : 0` bytes and zero-fills the rest.
+__device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async4z(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+// Arrive on the mbarrier once every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -255,31 +262,42 @@ __device__ __forceinline__ void dequant_half(const uint8_t* data, const uint8_t*
   }
 }
 
+// Nine warps: three share one SM sub-partition's register file, so the
+// launch bound holds each thread to 168 registers.
 template <kvq_format F>
 __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   using Tr = XTraits<F>;
   extern __shared__ uint8_t xsm_raw[];
-  __shared__ __align__(8) uint64_t bars[4];  // raw stage 0, raw stage 1, S ready, O ready
+  // mbarriers: per raw stage (landed), per slot (K/V tiles ready, S ready,
+  // P ready, PV done)
+  constexpr int kMaxRaw = 6;
+  __shared__ __align__(8) uint64_t bars[kMaxRaw + 4 * kSlots];
   __shared__ uint32_t tmem_slot;
   __shared__ int row_seq[kXRows];
   __shared__ int row_len[kXRows];
   __shared__ int pass_seq, pass_max, pass_bad, dead;
-  __shared__ uint32_t stage_ok[2];  // per raw stage: bit t set if tile t was copied
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool producer = warp >= 4;  // dequant warps 4-7 and the copy / MMA warp 8
+  const bool mma_warp = warp == 8;
   const int h = blockIdx.y, split = blockIdx.z;
   const long long R0 = (long long)blockIdx.x * kXRows;
   const uint32_t base_u32 = smem_u32(xsm_raw);
   uint8_t* sm = xsm_raw + (((base_u32 + 1023u) & ~1023u) - base_u32);
   const uint32_t sm_u32 = smem_u32(sm);
-  const uint32_t bar_raw0 = smem_u32(&bars[0]), bar_s = smem_u32(&bars[2]), bar_o = smem_u32(&bars[3]);
+  static_assert(Tr::kRaw <= kMaxRaw, "raw stages");
+  const uint32_t bar_raw = smem_u32(&bars[0]), bar_kv = smem_u32(&bars[kMaxRaw]);
+  const uint32_t bar_s = smem_u32(&bars[kMaxRaw + kSlots]), bar_p = smem_u32(&bars[kMaxRaw + 2 * kSlots]);
+  const uint32_t bar_o = smem_u32(&bars[kMaxRaw + 3 * kSlots]);
 
-  // ---- rows of this CTA: (query, q head) = divmod(R0 + tid, G) ----------------
-  const long long R = R0 + tid;
+  // ---- rows of this CTA (threads 0..127): (query, q head) = divmod(R0 + tid, G)
+  const int rho = tid & (kXRows - 1);
+  const long long R = R0 + rho;
   const long long qi = R / a.G;
   const bool qvalid = qi < a.n;
   const int qhead = h * a.G + (int)(R % a.G);
-  {
+  float qmul = 1.f;
+  if (!producer) {
     int s = -1, T = 0;
     if (qvalid) {
       s = __ldg(a.q_seq + qi);
@@ -289,15 +307,12 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
         s = -2;  // invalid: output zeros
       }
     }
-    row_seq[tid] = s;
-    row_len[tid] = T;
-  }
-  // ---- Q row -> 128B-swizzled K-major tile (two 64-element K atoms); for the
-  // f16 operand formats the row is scaled by 2^-sq so that its largest
-  // magnitude lies in [2^14, 2^15) and every bf16 value of it is exact in f16
-  // (2^sq joins the row's logit scale) ----------------------------------------
-  float qmul = 1.f;
-  {
+    row_seq[rho] = s;
+    row_len[rho] = T;
+    // Q row -> 128B-swizzled K-major tile (two 64-element K atoms); for the
+    // f16 operand formats the row is scaled by 2^-sq so that its largest
+    // magnitude lies in [2^14, 2^15) and every bf16 value of it is exact in
+    // f16 (2^sq joins the row's logit scale)
     const uint4* src = reinterpret_cast<const uint4*>(a.q + ((qvalid ? qi : 0) * a.Hq + qhead) * kHeadDim);
     uint4 qv[16];
 #pragma unroll
@@ -331,10 +346,16 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
     }
 #pragma unroll
     for (int c = 0; c < 16; ++c)
-      *reinterpret_cast<uint4*>(sm + kSQ + (c >> 3) * (kXRows * 128) + sw_off(tid, c & 7)) = qv[c];
+      *reinterpret_cast<uint4*>(sm + kSQ + (c >> 3) * (kXRows * 128) + sw_off(rho, c & 7)) = qv[c];
   }
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    // K/V ready and P ready collect one arrival per dequant / row warp
+    // raw stages: one arrival per dequant thread (its copies landed); K/V and
+    // P ready: one per dequant / row warp
+    for (int i = 0; i < kMaxRaw + 4 * kSlots; ++i) {
+      const int grp = i < kMaxRaw ? -1 : (i - kMaxRaw) / kSlots;  // 0 K/V, 1 S, 2 P, 3 O
+      mbar_init(smem_u32(&bars[i]), grp < 0 ? 128 : (grp == 0 || grp == 2) ? 4 : 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     dead = 0;
   }
@@ -348,7 +369,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
 
   const float cs = (a.kfac ? a.qscale * __ldg(a.kfac + h) : a.qscale) * qmul;
   const float vf = a.vfac ? __ldg(a.vfac + h) : a.v_factor;
@@ -356,17 +377,19 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   constexpr uint32_t kIdQK = idesc_16(kBf, kChunk, kXRows, 0);
   constexpr uint32_t kIdPV = idesc_16(kBf, 64, kXRows, 1);
 
-  uint32_t n_raw_issued = 0, n_raw_used = 0, n_s = 0, n_o = 0;
+  // chunk counters over the CTA's life: chunk number k uses raw stage, K/V
+  // slot and S slot k % 3, with mbarrier phase parity (k / 3) & 1
+  uint32_t k_next = 0;  // first chunk number of the current pass
   bool row_done = false;
 
   // ---- one pass per distinct sequence among the CTA's rows -------------------
   for (;;) {
     if (tid == 0) {
       int s = -1;
-      for (int rho = 0; rho < kXRows && s < 0; ++rho) s = row_seq[rho] >= 0 ? row_seq[rho] : -1;
+      for (int r2 = 0; r2 < kXRows && s < 0; ++r2) s = row_seq[r2] >= 0 ? row_seq[r2] : -1;
       int mx = 0;
-      for (int rho = 0; rho < kXRows; ++rho)
-        if (row_seq[rho] == s && s >= 0) mx = max(mx, row_len[rho]);
+      for (int r2 = 0; r2 < kXRows; ++r2)
+        if (row_seq[r2] == s && s >= 0) mx = max(mx, row_len[r2]);
       pass_seq = s;
       pass_max = mx;
       pass_bad = 0;
@@ -375,239 +398,267 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
     const int s = pass_seq;
     if (s < 0 || dead) break;
     const int maxT = pass_max;
-    const bool act = row_seq[tid] == s;
-    const int Tr_ = row_len[tid];
     const int32_t* prow = a.page_table + (long long)s * a.max_pages;
     const int nc = (maxT + kChunk - 1) / kChunk;
     const int c0 = (int)((long long)nc * split / a.splits), c1 = (int)((long long)nc * (split + 1) / a.splits);
+    const uint32_t kbase = k_next;
+    const int nch = c1 - c0;
+    k_next += (uint32_t)max(nch, 0);
 
-    // issue the raw copies of chunk c into ring stage st (warp 0); chunks go
-    // through the two stages in order, so chunk number k (counted over the
-    // CTA's life) uses stage k & 1 with mbarrier phase parity (k >> 1) & 1
-    auto issue = [&](int c, uint32_t st) {
-      const uint32_t bar = bar_raw0 + 8 * st;
-      const uint32_t dst0 = sm_u32 + kSRaw + st * Tr::kStage;
-      const int t = lane >> 2, kind = lane & 3;  // lanes 0..15: tile t, tensor kind
-      bool mine = false;
-      uint32_t bytes = 0;
-      const uint8_t* src = nullptr;
-      uint32_t dst = 0;
-      bool bad = false;
-      if (lane < 16 && (kind < 2 || Tr::kScales)) {
-        const int tok0 = c * kChunk + 16 * t;
-        if (tok0 < maxT) {
-          const int page = __ldg(prow + tok0 / a.P);
-          if (page >= 0 && page < a.num_pages) {
-            const long long rowi = ((long long)page * a.H + h) * a.P + tok0 % a.P;
-            const int rb = kind < 2 ? Tr::kRow : 8;
-            const uint8_t* pool = kind == 0 ? a.kd : kind == 1 ? a.vd : kind == 2 ? a.ks : a.vs;
-            src = pool + rowi * rb;
-            bytes = 16u * rb;
-            dst = dst0 + (kind == 0 ? 0 : kind == 1 ? Tr::kData : kind == 2 ? 2 * Tr::kData
-                                                                             : 2 * Tr::kData + Tr::kScl) +
-                  t * 16 * rb;
-            mine = true;
+    if (mma_warp) {
+      // ================= MMA warp: QK^T and PV issue ==========================
+      // O += P V of chunk number kk once its P is ready (acc == 0 starts the pass)
+      auto issue_pv = [&](uint32_t kk, bool start) -> bool {
+        const uint32_t slot = kk % kSlots;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_p + 8 * slot, (kk / kSlots) & 1u));
+        if (!ok) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t pcol = tmem + kColS + 64 * slot;
+          const uint32_t vbase = sm_u32 + kSKV + slot * 2 * kTileKV + kTileKV;
+#pragma unroll
+          for (int j = 0; j < kChunk / 16; ++j) {
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+              const uint64_t bd = sw128_desc(vbase + nh * (kChunk * 128) + j * 2048, 1024);
+              const uint32_t d = tmem + kColO + 64 * nh;
+              mma_ts(d, pcol + 8 * j, bd, kIdPV, (start && j == 0) ? 0u : 1u);
+              if (!Tr::kF16) mma_ts(d, pcol + 32 + 8 * j, bd, kIdPV, 1u);
+            }
+          }
+          mma_commit(bar_o + 8 * slot);
+        }
+        __syncwarp();
+        return true;
+      };
+
+      for (int c = c0; c < c1; ++c) {
+        const uint32_t kk = kbase + (uint32_t)(c - c0), slot = kk % kSlots;
+        // K/V tiles of chunk kk dequantized
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_kv + 8 * slot, (kk / kSlots) & 1u))) {
+          if (lane == 0) dead = 1;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          // S = Q K^T into S slot `slot`
+          const uint32_t kb = sm_u32 + kSKV + slot * 2 * kTileKV;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint64_t ad = sw128_desc(sm_u32 + kSQ + (j >> 2) * (kXRows * 128) + (j & 3) * 32, 1024);
+            const uint64_t bd = sw128_desc(kb + (j >> 2) * (kChunk * 128) + (j & 3) * 32, 1024);
+            mma_ss(tmem + kColS + 64 * slot, ad, bd, kIdQK, j > 0);
+          }
+          mma_commit(bar_s + 8 * slot);
+        }
+        __syncwarp();
+        // then O += P V of the previous chunk, once its P is ready
+        if (c > c0 && !issue_pv(kk - 1, c - 1 == c0)) {
+          if (lane == 0) dead = 1;
+          break;
+        }
+      }
+      if (nch > 0 && !dead && !issue_pv(kbase + (uint32_t)(nch - 1), nch == 1) && lane == 0) dead = 1;
+    } else if (producer) {
+      // ======== dequant warps: raw copies, raw stage -> swizzled K/V tiles ========
+      // Thread (token tt of the chunk, head_dim half hf) copies its own slice
+      // of each chunk (K and V half rows and their block scales) into the raw
+      // stage with cp.async, kRaw chunks ahead, and is the only thread that
+      // reads that slice back; a stage's mbarrier completes once all 128
+      // threads' copies have landed.  Absent tokens and bad pages zero-fill.
+      const int ptid = tid - 128, tt = ptid >> 1, hf = ptid & 1;
+      auto page_of = [&](int c) -> int {
+        const int tok = c * kChunk + tt;
+        return (c < c1 && tok < maxT) ? __ldg(prow + tok / a.P) : -1;
+      };
+      auto fill = [&](int c, uint32_t st, int page) {
+        const int tok = c * kChunk + tt;
+        const bool in_seq = tok < maxT;
+        const bool ok = in_seq && page >= 0 && page < a.num_pages;
+        if (in_seq && !ok) pass_bad = 1;
+        const long long rowi = ok ? ((long long)page * a.H + h) * a.P + tok % a.P : 0;
+        const uint32_t stage = sm_u32 + kSRaw + st * Tr::kStage;
+        constexpr int kHalf = Tr::kRow / 2;
+        const uint32_t dk = stage + tt * Tr::kRow + hf * kHalf;
+        const uint8_t* sk = a.kd + rowi * Tr::kRow + hf * kHalf;
+        const uint8_t* sv = a.vd + rowi * Tr::kRow + hf * kHalf;
+#pragma unroll
+        for (int i = 0; i < kHalf / 16; ++i) {
+          cp_async16z(dk + 16 * i, sk + 16 * i, ok);
+          cp_async16z(dk + Tr::kData + 16 * i, sv + 16 * i, ok);
+        }
+        if constexpr (Tr::kScales) {
+          const uint32_t ds = stage + 2 * Tr::kData + tt * 8 + hf * 4;
+          cp_async4z(ds, a.ks + rowi * 8 + hf * 4, ok);
+          cp_async4z(ds + Tr::kScl, a.vs + rowi * 8 + hf * 4, ok);
+        }
+        cp_async_arrive(bar_raw + 8 * st);
+      };
+      for (int c = c0; c < min(c0 + Tr::kRaw, c1); ++c)
+        fill(c, (kbase + (uint32_t)(c - c0)) % Tr::kRaw, page_of(c));
+      int next_page = page_of(c0 + Tr::kRaw);  // page of the chunk the next refill copies
+      for (int c = c0; c < c1; ++c) {
+        const uint32_t kk = kbase + (uint32_t)(c - c0), slot = kk % kSlots;
+        // raw chunk landed; K/V slot and S slot free (PV of chunk kk - 3 done)
+        const uint32_t rst = kk % Tr::kRaw;
+        bool ok = mbar_wait_bounded(bar_raw + 8 * rst, (kk / Tr::kRaw) & 1u);
+        if (ok && c - c0 >= kSlots) ok = mbar_wait_bounded(bar_o + 8 * slot, ((kk - kSlots) / kSlots) & 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) dead = 1;
+          break;
+        }
+        tc_fence_after();
+        {
+          const uint8_t* stage = sm + kSRaw + rst * Tr::kStage;
+          const bool tok_ok = c * kChunk + tt < maxT;
+          uint32_t kw[32], vw[32];
+          if (tok_ok) {
+            dequant_half<F>(stage, stage + 2 * Tr::kData, tt, hf, kw);
+            dequant_half<F>(stage + Tr::kData, stage + 2 * Tr::kData + Tr::kScl, tt, hf, vw);
           } else {
-            bad = true;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) kw[i] = vw[i] = 0u;
+          }
+          uint8_t* kv = sm + kSKV + slot * 2 * kTileKV;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const uint32_t off = hf * (kChunk * 128) + sw_off(tt, cc);
+            *reinterpret_cast<uint4*>(kv + off) = make_uint4(kw[4 * cc], kw[4 * cc + 1], kw[4 * cc + 2], kw[4 * cc + 3]);
+            *reinterpret_cast<uint4*>(kv + kTileKV + off) =
+                make_uint4(vw[4 * cc], vw[4 * cc + 1], vw[4 * cc + 2], vw[4 * cc + 3]);
           }
         }
-      }
-      const uint32_t okmask = __ballot_sync(0xffffffffu, mine && kind == 0);
-      uint32_t total = bytes;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-      if (__any_sync(0xffffffffu, bad) && lane == 0) pass_bad = 1;
-      if (lane == 0) {
-        uint32_t tiles = 0;
-        for (int tt = 0; tt < 4; ++tt) tiles |= ((okmask >> (4 * tt)) & 1u) << tt;
-        stage_ok[st] = tiles;
-        mbar_arrive_tx(bar, total);
-      }
-      __syncwarp();
-      if (mine) bulk_g2s(dst, src, bytes, bar);
-    };
-
-    float m = -INFINITY, l = 0.f;
-    bool first = true;
-    for (int c = c0; c < min(c0 + 2, c1); ++c) {
-      if (warp == 0) issue(c, n_raw_issued & 1u);
-      ++n_raw_issued;
-    }
-    for (int c = c0; c < c1; ++c) {
-      // ---- raw chunk c landed ----
-      const uint32_t st = n_raw_used & 1u;
-      const bool ok = mbar_wait_bounded(bar_raw0 + 8 * st, (n_raw_used >> 1) & 1u);
-      ++n_raw_used;
-      if (!ok) dead = 1;
-      // ---- dequantize chunk c into the swizzled bf16 K and V tiles ----
-      {
-        const uint8_t* stage = sm + kSRaw + st * Tr::kStage;
-        const int tt = tid >> 1, hf = tid & 1;
-        const bool tok_ok = ((stage_ok[st] >> (tt >> 4)) & 1u) && c * kChunk + tt < maxT;
-        uint32_t kw[32], vw[32];
-        if (tok_ok) {
-          dequant_half<F>(stage, stage + 2 * Tr::kData, tt, hf, kw);
-          dequant_half<F>(stage + Tr::kData, stage + 2 * Tr::kData + Tr::kScl, tt, hf, vw);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) kw[i] = vw[i] = 0u;
-        }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint32_t off = hf * (kChunk * 128) + sw_off(tt, cc);
-          *reinterpret_cast<uint4*>(sm + kSK + off) = make_uint4(kw[4 * cc], kw[4 * cc + 1], kw[4 * cc + 2], kw[4 * cc + 3]);
-          *reinterpret_cast<uint4*>(sm + kSV + off) = make_uint4(vw[4 * cc], vw[4 * cc + 1], vw[4 * cc + 2], vw[4 * cc + 3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_kv + 8 * slot) : "memory");
+        // refill this thread's slice of the stage just read with chunk c + kRaw
+        if (c + Tr::kRaw < c1) {
+          fill(c + Tr::kRaw, rst, next_page);
+          next_page = page_of(c + Tr::kRaw + 1);
         }
       }
-      fence_proxy_async();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (dead) break;
-      // ---- refill the consumed stage with chunk c + 2 ----
-      if (c + 2 < c1) {
-        if (warp == 0) {
-          fence_proxy_async();
-          issue(c + 2, n_raw_issued & 1u);
+    } else {
+      // ================= rows: online softmax, O rescale, epilogue =============
+      const bool act = row_seq[rho] == s;
+      const int Tr_ = row_len[rho];
+      float m = -INFINITY, l = 0.f;
+      for (int c = c0; c < c1; ++c) {
+        const uint32_t kk = kbase + (uint32_t)(c - c0), slot = kk % kSlots;
+        const bool sok = mbar_wait_bounded(bar_s + 8 * slot, (kk / kSlots) & 1u);
+        tc_fence_after();
+        if (!__all_sync(0xffffffffu, sok)) {
+          if (lane == 0) dead = 1;
+          break;
         }
-        ++n_raw_issued;
-      }
-      // ---- S = Q K^T ----
-      if (tid == 0) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint64_t ad = sw128_desc(sm_u32 + kSQ + (j >> 2) * (kXRows * 128) + (j & 3) * 32, 1024);
-          const uint64_t bd = sw128_desc(sm_u32 + kSK + (j >> 2) * (kChunk * 128) + (j & 3) * 32, 1024);
-          mma_ss(tmem + kColS, ad, bd, kIdQK, j > 0);
-        }
-        mma_commit(bar_s);
-      }
-      const bool sok = mbar_wait_bounded(bar_s, n_s & 1u);
-      ++n_s;
-      tc_fence_after();
-      if (!__all_sync(0xffffffffu, sok)) {
-        if (lane == 0) dead = 1;
-      }
-      // ---- online softmax of this thread's row ----
-      uint32_t sv[64];
-      {
-        uint32_t t0[32], t1[32];
-        tmem_ld32(tmem + lane_off + kColS, t0);
-        tmem_ld32(tmem + lane_off + kColS + 32, t1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          sv[j] = t0[j];
-          sv[32 + j] = t1[j];
-        }
-      }
-      float mx = -INFINITY;
-      if (act && (c + 1) * kChunk <= Tr_) {  // every token of the chunk is in this row's prefix
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float x = __uint_as_float(sv[j]) * cs;
-          sv[j] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int tok = c * kChunk + j;
-          const float x = (act && tok < Tr_) ? __uint_as_float(sv[j]) * cs : -INFINITY;
-          sv[j] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
-      }
-      const bool grow = mx > m + 8.f;
-      const float m_new = grow ? mx : m;
-      // rescale what O already holds (warp-uniform tensor-memory access)
-      if (__any_sync(0xffffffffu, grow && m != -INFINITY && !first)) {
-        const float al = (grow && m != -INFINITY) ? ex2x(m - m_new) : 1.f;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t ov[32];
-          tmem_ld32(tmem + lane_off + kColO + 32 * q4, ov);
+        const uint32_t scol = tmem + lane_off + kColS + 64 * slot;
+        uint32_t sv[64];
+        {
+          uint32_t t0[32], t1[32];
+          tmem_ld32(scol, t0);
+          tmem_ld32(scol + 32, t1);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * al);
-          tmem_st32(tmem + lane_off + kColO + 32 * q4, ov);
-        }
-        l *= al;
-      } else if (grow && m != -INFINITY) {
-        l *= ex2x(m - m_new);
-      }
-      m = m_new;
-      if constexpr (Tr::kF16) {
-        // P <= 2^8 in f16 (relative rounding 2^-11)
-        uint32_t ph[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x0 = __uint_as_float(sv[2 * j]), x1 = __uint_as_float(sv[2 * j + 1]);
-          const float p0 = (x0 == -INFINITY) ? 0.f : ex2x(x0 - m);
-          const float p1 = (x1 == -INFINITY) ? 0.f : ex2x(x1 - m);
-          l += p0 + p1;
-          uint32_t r;
-          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));
-          ph[j] = r;
-        }
-        tmem_st32(tmem + lane_off + kColPh, ph);
-        tmem_wait_st();
-      } else {
-        uint32_t ph[32], pl[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x0 = __uint_as_float(sv[2 * j]), x1 = __uint_as_float(sv[2 * j + 1]);
-          const float p0 = (x0 == -INFINITY) ? 0.f : ex2x(x0 - m);
-          const float p1 = (x1 == -INFINITY) ? 0.f : ex2x(x1 - m);
-          l += p0 + p1;
-          ph[j] = bf2(p0, p1);
-          const float r0 = p0 - bf16_bits_to_float(ph[j] & 0xFFFFu);
-          const float r1 = p1 - bf16_bits_to_float(ph[j] >> 16);
-          pl[j] = bf2(r0, r1);
-        }
-        tmem_st32(tmem + lane_off + kColPh, ph);
-        tmem_st32(tmem + lane_off + kColPl, pl);
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (dead) break;
-      // ---- O += P V (two 64-column halves of head_dim; P high and low parts) ----
-      if (tid == 0) {
-#pragma unroll
-        for (int j = 0; j < kChunk / 16; ++j) {
-#pragma unroll
-          for (int nh = 0; nh < 2; ++nh) {
-            const uint64_t bd = sw128_desc(sm_u32 + kSV + nh * (kChunk * 128) + j * 2048, 1024);
-            const uint32_t d = tmem + kColO + 64 * nh;
-            mma_ts(d, tmem + kColPh + 8 * j, bd, kIdPV, (first && j == 0) ? 0u : 1u);
-            if (!Tr::kF16) mma_ts(d, tmem + kColPl + 8 * j, bd, kIdPV, 1u);
+          for (int j = 0; j < 32; ++j) {
+            sv[j] = t0[j];
+            sv[32 + j] = t1[j];
           }
         }
-        mma_commit(bar_o);
+        float mx = -INFINITY;
+        if (act && (c + 1) * kChunk <= Tr_) {  // every token of the chunk is in this row's prefix
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const float x = __uint_as_float(sv[j]) * cs;
+            sv[j] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const int tok = c * kChunk + j;
+            const float x = (act && tok < Tr_) ? __uint_as_float(sv[j]) * cs : -INFINITY;
+            sv[j] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        }
+        const bool grow = mx > m + 8.f;
+        const float m_new = grow ? mx : m;
+        if (__any_sync(0xffffffffu, grow && m != -INFINITY && c > c0)) {
+          // rescale what O holds: the PV of the previous chunk must be done
+          const uint32_t kp = kk - 1;
+          const bool pok = mbar_wait_bounded(bar_o + 8 * (kp % kSlots), (kp / kSlots) & 1u);
+          tc_fence_after();
+          if (!__all_sync(0xffffffffu, pok)) {
+            if (lane == 0) dead = 1;
+            break;
+          }
+          const float al = (grow && m != -INFINITY) ? ex2x(m - m_new) : 1.f;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + lane_off + kColO + 32 * q4, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * al);
+            tmem_st32(tmem + lane_off + kColO + 32 * q4, ov);
+          }
+          l *= al;
+        } else if (grow && m != -INFINITY) {
+          l *= ex2x(m - m_new);
+        }
+        m = m_new;
+        // P over this chunk's S slot
+        if constexpr (Tr::kF16) {
+          uint32_t ph[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x0 = __uint_as_float(sv[2 * j]), x1 = __uint_as_float(sv[2 * j + 1]);
+            const float p0 = (x0 == -INFINITY) ? 0.f : ex2x(x0 - m);
+            const float p1 = (x1 == -INFINITY) ? 0.f : ex2x(x1 - m);
+            l += p0 + p1;
+            uint32_t r;
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));
+            ph[j] = r;
+          }
+          tmem_st32(scol, ph);
+        } else {
+          uint32_t ph[32], pl[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x0 = __uint_as_float(sv[2 * j]), x1 = __uint_as_float(sv[2 * j + 1]);
+            const float p0 = (x0 == -INFINITY) ? 0.f : ex2x(x0 - m);
+            const float p1 = (x1 == -INFINITY) ? 0.f : ex2x(x1 - m);
+            l += p0 + p1;
+            ph[j] = bf2(p0, p1);
+            const float r0 = p0 - bf16_bits_to_float(ph[j] & 0xFFFFu);
+            const float r1 = p1 - bf16_bits_to_float(ph[j] >> 16);
+            pl[j] = bf2(r0, r1);
+          }
+          tmem_st32(scol, ph);
+          tmem_st32(scol + 32, pl);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_p + 8 * slot) : "memory");
       }
-      const bool ook = mbar_wait_bounded(bar_o, n_o & 1u);
-      ++n_o;
-      tc_fence_after();
-      if (!__all_sync(0xffffffffu, ook)) {
-        if (lane == 0) dead = 1;
+      // ---- O of this pass complete (last PV done); partial or final output ----
+      bool has_o = false;
+      if (nch > 0 && !dead) {
+        const uint32_t kl = kbase + (uint32_t)(nch - 1);
+        const bool ook = mbar_wait_bounded(bar_o + 8 * (kl % kSlots), (kl / kSlots) & 1u);
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, ook)) has_o = true;
+        else if (lane == 0) dead = 1;
       }
-      first = false;
-    }
-    __syncthreads();
-    // ---- this pass's rows: partial (or final) output of this split ----
-    const bool poison = pass_bad != 0 || dead != 0;
-    if (pass_bad && tid == 0) atomicOr(a.err, kErrRange);
-    if (dead && tid == 0) atomicOr(a.err, kErrTimeout);
-    {
-      const bool has = !first && l > 0.f;
+      has_o = __all_sync(0xffffffffu, has_o);
+      const bool poison = pass_bad != 0 || dead != 0;
+      const bool has = has_o && l > 0.f;
       const float inv = (has && !poison) ? vf / l : 0.f;
       const long long rowg = qi * a.Hq + qhead;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t ov[32];
-        if (!first) {  // warp-uniform: every thread of the pass has run the chunks
+        if (has_o) {  // warp-uniform
           tmem_ld32(tmem + lane_off + kColO + 32 * q4, ov);
           tmem_wait_ld();
         } else {
@@ -637,13 +688,16 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0)
-      for (int rho = 0; rho < kXRows; ++rho)
-        if (row_seq[rho] == s) row_seq[rho] = -1;
+    if (tid == 0) {
+      if (pass_bad) atomicOr(a.err, kErrRange);
+      for (int r2 = 0; r2 < kXRows; ++r2)
+        if (row_seq[r2] == s) row_seq[r2] = -1;
+    }
     __syncthreads();
   }
+  if (tid == 0 && dead) atomicOr(a.err, kErrTimeout);
   // rows that never ran (invalid, or left after a wait ran out): zero output
-  if (qvalid && !row_done) {
+  if (!producer && qvalid && !row_done) {
     const long long rowg = qi * a.Hq + qhead;
     if (a.splits == 1) {
       uint4* dst = reinterpret_cast<uint4*>(a.out + rowg * kHeadDim);
@@ -653,12 +707,15 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
       a.part_lse[rowg * a.splits + split] = dead ? INFINITY : -INFINITY;
     }
   }
-  // copies and MMAs still in flight (after a wait ran out): give them a
-  // bounded chance to complete before the CTA frees its tensor memory and exits
-  if (dead) {
-    for (uint32_t t = n_raw_used; t < n_raw_issued; ++t) mbar_wait_bounded(bar_raw0 + 8 * (t & 1u), (t >> 1) & 1u);
-    if (n_s > 0) mbar_wait_bounded(bar_s, (n_s - 1) & 1u);
-    if (n_o > 0) mbar_wait_bounded(bar_o, (n_o - 1) & 1u);
+  // after a wait ran out: give copies and MMAs still in flight a bounded
+  // chance to complete before the CTA frees its tensor memory and exits
+  if (dead && mma_warp) {
+    const uint32_t k0 = k_next > kSlots ? k_next - kSlots : 0;
+    for (uint32_t t = k0; t < k_next; ++t) {
+      mbar_wait_bounded(bar_raw + 8 * (t % Tr::kRaw), (t / Tr::kRaw) & 1u);
+      mbar_wait_bounded(bar_s + 8 * (t % kSlots), (t / kSlots) & 1u);
+      mbar_wait_bounded(bar_o + 8 * (t % kSlots), (t / kSlots) & 1u);
+    }
   }
   tc_fence_before();
   __syncthreads();
