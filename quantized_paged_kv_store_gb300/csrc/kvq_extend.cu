@@ -39,29 +39,29 @@
 #include "kvq_internal.h"
 
 #include <algorithm>
+#include <cmath>
 
 namespace kvq {
 namespace {
 
 constexpr int kXRows = 128;        // (query, q head) rows per CTA = TMEM lanes
-constexpr int kXThreads = 288;     // warps 0-3: rows; 4-7: dequant; 8: copies and MMA issue
-constexpr int kSlots = 3;          // raw stages, K/V tiles and S slots in flight
+constexpr int kXThreads = 288;     // warps 0-3: rows; 4-7: dequant; 8: MMA issue
+constexpr int kMaxSlots = 4;       // K/V tiles and S slots in flight (per format below)
 constexpr int kChunk = 64;         // tokens per chunk (four 16-token tiles)
 constexpr int kMaxSplits = 16;
 constexpr uint32_t kXWaitLimit = 1u << 22;
 
-// tensor-memory columns: three S slots (64 fp32 columns each; P of a chunk
-// is written back over its own S slot: f16 in 32 columns, or bf16 high and
-// low parts in 64) and O (128 fp32 columns, two halves of head_dim)
+// tensor-memory columns: up to four S slots (64 fp32 columns each; P of a
+// chunk is written back over its own S slot: f16 in 32 columns, or bf16 high
+// and low parts in 64) and O (128 fp32 columns, two halves of head_dim)
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 64 * kSlots;
+constexpr uint32_t kColO = 64 * kMaxSlots;
 constexpr uint32_t kTmemCols = 512;
 
 // shared memory (dynamic, 1024-byte aligned offsets)
 constexpr int kSQ = 0;                              // Q: 2 K-atoms x 128 rows x 128 B
 constexpr int kSKV = kSQ + 2 * kXRows * 128;        // slots of [K tile | V tile]
 constexpr int kTileKV = 2 * kChunk * 128;           // one K (or V) tile: 2 atoms x 64 tokens x 128 B
-constexpr int kSRaw = kSKV + kSlots * 2 * kTileKV;  // raw stages
 
 template <kvq_format F>
 struct XTraits {
@@ -75,8 +75,10 @@ struct XTraits {
   static constexpr int kData = kChunk * kRow;
   static constexpr int kScl = kScales ? kChunk * 8 : 0;
   static constexpr int kStage = 2 * kData + 2 * kScl;
-  // raw stages in flight: as many as shared memory leaves room for
+  // K/V and S slots and raw stages in flight: as many as shared memory holds
+  static constexpr int kSlots = (F == KVQ_BF16) ? 3 : 4;
   static constexpr int kRaw = (F == KVQ_BF16) ? 3 : (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) ? 4 : 6;
+  static constexpr int kSRaw = kSKV + kSlots * 2 * kTileKV;  // raw stages
   static constexpr int kSmem = kSRaw + kRaw * kStage + 1024;  // + alignment slack
 };
 
@@ -271,7 +273,9 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   // mbarriers: per raw stage (landed), per slot (K/V tiles ready, S ready,
   // P ready, PV done)
   constexpr int kMaxRaw = 6;
-  __shared__ __align__(8) uint64_t bars[kMaxRaw + 4 * kSlots];
+  constexpr int kSlots = Tr::kSlots;
+  constexpr int kSRaw = Tr::kSRaw;
+  __shared__ __align__(8) uint64_t bars[kMaxRaw + 4 * kMaxSlots];
   __shared__ uint32_t tmem_slot;
   __shared__ int row_seq[kXRows];
   __shared__ int row_len[kXRows];
@@ -287,8 +291,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   const uint32_t sm_u32 = smem_u32(sm);
   static_assert(Tr::kRaw <= kMaxRaw, "raw stages");
   const uint32_t bar_raw = smem_u32(&bars[0]), bar_kv = smem_u32(&bars[kMaxRaw]);
-  const uint32_t bar_s = smem_u32(&bars[kMaxRaw + kSlots]), bar_p = smem_u32(&bars[kMaxRaw + 2 * kSlots]);
-  const uint32_t bar_o = smem_u32(&bars[kMaxRaw + 3 * kSlots]);
+  const uint32_t bar_s = smem_u32(&bars[kMaxRaw + kMaxSlots]), bar_p = smem_u32(&bars[kMaxRaw + 2 * kMaxSlots]);
+  const uint32_t bar_o = smem_u32(&bars[kMaxRaw + 3 * kMaxSlots]);
 
   // ---- rows of this CTA (threads 0..127): (query, q head) = divmod(R0 + tid, G)
   const int rho = tid & (kXRows - 1);
@@ -352,8 +356,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
     // K/V ready and P ready collect one arrival per dequant / row warp
     // raw stages: one arrival per dequant thread (its copies landed); K/V and
     // P ready: one per dequant / row warp
-    for (int i = 0; i < kMaxRaw + 4 * kSlots; ++i) {
-      const int grp = i < kMaxRaw ? -1 : (i - kMaxRaw) / kSlots;  // 0 K/V, 1 S, 2 P, 3 O
+    for (int i = 0; i < kMaxRaw + 4 * kMaxSlots; ++i) {
+      const int grp = i < kMaxRaw ? -1 : (i - kMaxRaw) / kMaxSlots;  // 0 K/V, 1 S, 2 P, 3 O
       mbar_init(smem_u32(&bars[i]), grp < 0 ? 128 : (grp == 0 || grp == 2) ? 4 : 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -377,8 +381,9 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   constexpr uint32_t kIdQK = idesc_16(kBf, kChunk, kXRows, 0);
   constexpr uint32_t kIdPV = idesc_16(kBf, 64, kXRows, 1);
 
-  // chunk counters over the CTA's life: chunk number k uses raw stage, K/V
-  // slot and S slot k % 3, with mbarrier phase parity (k / 3) & 1
+  // chunk counters over the CTA's life: chunk number k uses raw stage
+  // k % kRaw and K/V and S slot k % kSlots, with mbarrier phase parity
+  // (k / kRaw) & 1 and (k / kSlots) & 1
   uint32_t k_next = 0;  // first chunk number of the current pass
   bool row_done = false;
 
@@ -499,8 +504,14 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
       int next_page = page_of(c0 + Tr::kRaw);  // page of the chunk the next refill copies
       for (int c = c0; c < c1; ++c) {
         const uint32_t kk = kbase + (uint32_t)(c - c0), slot = kk % kSlots;
-        // raw chunk landed; K/V slot and S slot free (PV of chunk kk - 3 done)
         const uint32_t rst = kk % Tr::kRaw;
+        // refill this thread's slice of the stage read in the previous
+        // iteration with chunk c - 1 + kRaw (issued before this chunk's work)
+        if (c > c0 && c - 1 + Tr::kRaw < c1) {
+          fill(c - 1 + Tr::kRaw, (kk - 1) % Tr::kRaw, next_page);
+          next_page = page_of(c + Tr::kRaw);
+        }
+        // raw chunk landed; K/V slot and S slot free (PV of chunk kk - kSlots done)
         bool ok = mbar_wait_bounded(bar_raw + 8 * rst, (kk / Tr::kRaw) & 1u);
         if (ok && c - c0 >= kSlots) ok = mbar_wait_bounded(bar_o + 8 * slot, ((kk - kSlots) / kSlots) & 1u);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -531,11 +542,6 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_kv + 8 * slot) : "memory");
-        // refill this thread's slice of the stage just read with chunk c + kRaw
-        if (c + Tr::kRaw < c1) {
-          fill(c + Tr::kRaw, rst, next_page);
-          next_page = page_of(c + Tr::kRaw + 1);
-        }
       }
     } else {
       // ================= rows: online softmax, O rescale, epilogue =============
@@ -785,10 +791,20 @@ int extend_splits(const Geometry& g, int num_q_tokens, int num_q_heads, int max_
   const int G = num_q_heads / g.kv_heads;
   const long long ctas = (((long long)num_q_tokens * G + kXRows - 1) / kXRows) * g.kv_heads;
   const long long chunks = ((long long)max_pages_per_seq * g.page_size + kChunk - 1) / kChunk;
-  // about four CTAs per SM over the grid, at least four chunks per split
-  long long s = ctas > 0 ? (4LL * sms + ctas - 1) / ctas : 1;
-  s = std::min<long long>(s, std::max<long long>(1, chunks / 4));
-  return (int)std::max<long long>(1, std::min<long long>(s, kMaxSplits));
+  if (ctas <= 0) return 1;
+  // one CTA per SM: at least two waves, at least 16 chunks per split, and the
+  // split count whose last wave is fullest (waves / ceil(waves) >= 0.9)
+  const long long s_max = std::max<long long>(1, std::min<long long>(kMaxSplits, chunks / 16));
+  const long long s_min = std::min<long long>(s_max, std::max<long long>(1, (2LL * sms + ctas - 1) / ctas));
+  long long best = s_min;
+  double best_eff = 0.0;
+  for (long long s = s_min; s <= s_max; ++s) {
+    const double waves = (double)(ctas * s) / sms;
+    const double eff = waves / std::ceil(waves);
+    if (eff >= 0.9) return (int)s;
+    if (eff > best_eff) { best_eff = eff; best = s; }
+  }
+  return (int)best;
 }
 
 size_t extend_workspace_bytes(int splits, int num_q_tokens, int num_q_heads) {
