@@ -131,6 +131,16 @@ def peak_hbm():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def peak_bf16():
+    """Measured dense bf16 tensor TFLOP/s (burst) from MEASURED_PEAKS.json, else
+    the 1915 TFLOP/s fallback of an earlier GB300 measurement."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, ValueError, KeyError, TypeError):
+        return 1915.0, "fallback"
+
+
 def decode_source_hash():
     h = hashlib.sha256()
     for n in ("kvq_decode.cu", "kvq_decode_args.cuh", "kvq_codecs.cuh"):
@@ -762,7 +772,8 @@ def run_next(args):
     d_qs, d_ql = torch.from_numpy(q_seq).to(dev), torch.from_numpy(q_len).to(dev)
     d_pt = torch.from_numpy(wl.page_table).to(dev)
     d_out = torch.empty_like(d_q)
-    ws = torch.empty(cache.workspace_size(len(q_seq), wl.Hq, wl.max_pages), dtype=torch.uint8, device=dev)
+    wsb = kvq.kvq_extend_workspace_size(cache.handle, len(q_seq), wl.Hq, wl.max_pages)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
     ms = _time_calls(lambda: cache.extend_attention(0, d_q, d_qs, d_ql, d_pt, wl.sm_scale, d_out, ws),
                      max(10, steps // 10), warm)
     if cache.device_error() != 0:
@@ -770,11 +781,17 @@ def run_next(args):
     prefix = int(wl.seq_lens.sum()) * wl.Hkv * KV_BYTES[fmt]
     qo = 2 * len(q_seq) * wl.Hq * wl.D * 2
     gbs = (prefix + qo) / (ms * 1e-3) / 1e9
+    # QK^T and PV: 2 * 128 multiply-adds per (query row, q head, context token) each
+    flops = float(q_len.astype(np.int64).sum()) * wl.Hq * wl.D * 4
+    tflops = flops / (ms * 1e-3) / 1e12
     emit({"path": "extend", "format": fmt, "workload": wl.name, "batch": wl.B, "chunk": chunk,
           "queries": len(q_seq), "ms_per_call": round(ms, 4),
           "queries_per_s": round(len(q_seq) / (ms * 1e-3), 1),
-          "GBps_prefix_once": round(gbs, 1), "frac": round(gbs / peak, 4),
-          "note": "each K/V tile dequantized once per 64 (query, q head) rows; bytes counted once per sequence"})
+          "TFLOPs": round(tflops, 1), "frac_tensor": round(tflops / peak_bf16()[0], 4),
+          "GBps_prefix_once": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
+          "workspace_bytes": wsb,
+          "note": "tcgen05 kernel: each 64-token K/V chunk dequantized once per 128 (query, q head) "
+                  "rows; the contraction is tensor-bound at 16 queries per sequence"})
     cache.close()
     return out
 

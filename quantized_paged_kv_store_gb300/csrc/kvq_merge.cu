@@ -23,9 +23,12 @@ constexpr int kMergeMaxWarps = 32;
 // workers (small batches) is merged by up to 32 warps.
 __global__ void __launch_bounds__(kMergeMaxWarps * 32) merge_kernel(DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ float4 s_acc[kMergeMaxWarps][32];
-  __shared__ float s_den[kMergeMaxWarps];
-  __shared__ float s_max[kMergeMaxWarps];
+  // dynamic: nwarps x (32 float4 + den + max), so small CTAs stay small
+  extern __shared__ float4 s_dyn[];
+  const int nw_cta = blockDim.x >> 5;
+  float4(*s_acc)[32] = reinterpret_cast<float4(*)[32]>(s_dyn);
+  float* s_den = reinterpret_cast<float*>(s_dyn + 32 * nw_cta);
+  float* s_max = s_den + nw_cta;
   const long long u = blockIdx.x / kGroupMax;
   const int g = (int)(blockIdx.x - u * kGroupMax);
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5, nwarps = blockDim.x >> 5;
@@ -138,7 +141,7 @@ cudaError_t launch_merge(const DecodeArgs& a, int64_t num_units, cudaStream_t st
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(num_units * kGroupMax));
   cfg.blockDim = dim3(32 * warps);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = warps > 1 ? (size_t)warps * (32 * sizeof(float4) + 2 * sizeof(float)) : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
