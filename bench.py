@@ -46,7 +46,8 @@ DTYPE = {"bf16": "bf16 cache; bf16 mma, f32 accumulate",
 # capture of the batch-8 case of the same workload scaled by units processed,
 # keyed by the hash of the split-kernel sources it was taken on: any change to
 # those sources reports null until re-measured.
-NCU_TRAFFIC = {("nvfp4", "4f7fbe551a3e635c"): 1086900000}
+NCU_TRAFFIC = {("nvfp4", "291f4699bb47f77f"): 1089570636,
+               ("fp4_mx_block16", "291f4699bb47f77f"): 1097894977}
 
 
 def parse_args(argv=None):
@@ -59,6 +60,9 @@ def parse_args(argv=None):
     p.add_argument("--seed", type=int, default=1004)
     p.add_argument("--sweep", default=None, help="also run the format x context x batch sweep, "
                    "one JSON line per cell appended to this file")
+    p.add_argument("--sweep-cells", default=None, help="comma-separated fmt:ctx:batch cells of "
+                   "the sweep to run (default: all)")
+    p.add_argument("--sweep-only", action="store_true", help="run only the --sweep measurement")
     p.add_argument("--store", default=None, help="also time quantize-and-store of the 70B-layer "
                    "16K x 8 prefill in every format, one JSON line per format appended to this file")
     p.add_argument("--store-formats", default=None, help="comma-separated subset for --store")
@@ -639,24 +643,84 @@ def run_store(args, steps=None, warmup=None):
                                     "frac": round(gbs / peak, 4)}) + "\n")
 
 
+def _graph_us(call, reps=20, replays=10):
+    """Device time per call: one CUDA graph of `reps` calls, replayed back to back."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(reps):
+                call(s)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * replays)
+
+
 def run_sweep(args):
-    rank, world, _ = dist_env()
+    """The format sweep on one 70B layer: contexts 4K / 16K / 32K x batch 1 / 8 /
+    32, every format (the K/V draws of a cell are shared by its formats).  Per
+    cell: mean CUDA-event time of one decode call issued from Python, and the
+    device time per call from CUDA-graph replay (no host launch cost)."""
+    import numpy as np
+    import torch
+    import quantized_paged_kv_store_gb300 as kvq
+    import synth
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
     peak, _ = peak_hbm()
-    for fmt in ("bf16", "fp8_e4m3", "fp8_e5m2", "fp4_mx_block16", "nvfp4"):
-        for T in (4096, 16384, 32768):
-            for B in (1, 8, 32):
-                a = argparse.Namespace(**vars(args))
-                a.steps = max(20, min(args.steps, 300))
-                r = run_cell(a, fmt, T=T, B=B, with_e2e=False)
-                ach = r["decode_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
+    want = None
+    if args.sweep_cells:
+        want = {tuple(c.split(":")) for c in args.sweep_cells.split(",")}
+    steps = max(20, min(args.steps, 300))
+    for T in (4096, 16384, 32768):
+        for B in (1, 8, 32):
+            fmts = [f for f in PER_FORMAT if want is None or (f, str(T), str(B)) in want]
+            if not fmts:
+                continue
+            wl = synth.cfg5_sweep_cell("bf16", T, B, seed=args.seed + 7919 * rank)
+            ks, vs = wl.kv_all(0)
+            kall, vall = synth_to_cuda(np.concatenate(ks)), synth_to_cuda(np.concatenate(vs))
+            slots = torch.from_numpy(np.concatenate([wl.slots(b) for b in range(wl.B)])).to(dev)
+            d_q = synth_to_cuda(wl.q(0))
+            d_pt = torch.from_numpy(wl.page_table).to(dev)
+            d_sl = torch.from_numpy(wl.seq_lens).to(dev)
+            for fmt in fmts:
+                cache = kvq.KVQCache(fmt, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
+                cache.quantize_and_store(0, kall, vall, slots, [float(x) for x in wl.scales_for(fmt, ks, vs)])
+                out = torch.empty_like(d_q)
+                ws = torch.empty(cache.workspace_size(wl.B, wl.Hq, wl.max_pages), dtype=torch.uint8,
+                                 device=dev)
+                ms = _time_calls(lambda: cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale, out, ws),
+                                 steps, 5)
+                gus = _graph_us(lambda st: cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale, out,
+                                                                  ws, stream=st))
+                if cache.device_error() != 0:
+                    raise RuntimeError(f"device error in sweep cell {fmt} {T} x {B}")
+                nb = algorithmic_bytes(wl, fmt)
                 if rank == 0:
                     with open(args.sweep, "a") as f:
-                        f.write(json.dumps({"format": fmt, "ctx": T, "batch": B,
-                                            "decode_us": round(r["decode_ms"] * 1e3, 2),
-                                            "step_us": round(r["ms"] * 1e3, 2),
-                                            "GBps": round(ach, 1), "frac": round(ach / peak, 4),
-                                            "tokens_per_s": round(B / (r["ms"] * 1e-3), 1),
-                                            "clocks": r["clocks"]}) + "\n")
+                        f.write(json.dumps({
+                            "format": fmt, "ctx": T, "batch": B,
+                            "decode_us": round(ms * 1e3, 2), "GBps": round(nb / (ms * 1e-3) / 1e9, 1),
+                            "frac": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
+                            "graph_us": round(gus, 2), "graph_GBps": round(nb / (gus * 1e-6) / 1e9, 1),
+                            "graph_frac": round(nb / (gus * 1e-6) / 1e9 / peak, 4),
+                            "tokens_per_s": round(B / (gus * 1e-6), 1)}) + "\n")
+                cache.close()
+            del kall, vall
 
 
 def _time_calls(fn, steps, warmup):
@@ -906,6 +970,9 @@ def main(argv=None):
     args = parse_args(argv)
     if args.store_only:
         run_store(args)
+        return
+    if args.sweep_only and args.sweep:
+        run_sweep(args)
         return
     if args.next:
         run_next(args)
