@@ -213,20 +213,14 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
     const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
     const uint32_t kr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     const uint32_t kr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-    float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      mma_f8<F>((j & 1) ? s2 : s, kr[2 * j], kr8[2 * j], kr[2 * j + 1], kr8[2 * j + 1], qb[j][0], qb[j][1]);
-    s[0] += s2[0];
-    s[1] += s2[1];
-    s[2] += s2[2];
-    s[3] += s2[3];
+      mma_f8<F>(s, kr[2 * j], kr8[2 * j], kr[2 * j + 1], kr8[2 * j + 1], qb[j][0], qb[j][1]);
   } else if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
     const uint4 x0 = lds128(sK + r * 128 + q * 32), x1 = lds128(sK + r * 128 + q * 32 + 16);
     const uint4 y0 = lds128(sK + (r + 8) * 128 + q * 32), y1 = lds128(sK + (r + 8) * 128 + q * 32 + 16);
     const uint32_t kr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     const uint32_t kr8[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-    float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: two independent MMA chains
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t a0, a1, a2, a3;
@@ -241,12 +235,8 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
         a1 = dec2_e5m2_h2(kr8[j]);
         a3 = dec2_e5m2_h2_hi(kr8[j]);
       }
-      mma_f16((j & 1) ? s2 : s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+      mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
     }
-    s[0] += s2[0];
-    s[1] += s2[1];
-    s[2] += s2[2];
-    s[3] += s2[3];
   } else if (F == KVQ_BF16) {
     uint32_t kr[16], kr8[16];
 #pragma unroll
@@ -277,7 +267,6 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
       f11 = kf[3];
     }
     const uint32_t kw[4] = {x.x, x.y, x.z, x.w}, kw8[4] = {y.x, y.y, y.z, y.w};
-    float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: two independent MMA chains
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t wr = kw[j >> 1], wr8 = kw8[j >> 1];
@@ -298,12 +287,8 @@ __device__ __forceinline__ void tile_qk(const uint8_t* sK, const uint8_t* sKs, i
       a2 = hmul2(a2, fr);
       a1 = hmul2(a1, fr8);
       a3 = hmul2(a3, fr8);
-      mma_f16((j & 1) ? s2 : s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
+      mma_f16(s, a0, a1, a2, a3, qb[j][0], qb[j][1]);
     }
-    s[0] += s2[0];
-    s[1] += s2[1];
-    s[2] += s2[2];
-    s[3] += s2[3];
   }
 
 }
