@@ -181,6 +181,7 @@ kvq_status kvq_calibrate_scales(kvq_cache* cache, int layer, const void* k_bf16,
  *   workspace:   device scratch of at least kvq_decode_workspace_size(...)
  *                bytes, 16-byte aligned, used only during the call (split-K
  *                partial outputs and log-sum-exps).
+ * sm_scale: any finite value (a negative one is folded into the query's sign).
  * Supported: head_dim == 128, page_size % 16 == 0, num_q_heads % kv_heads == 0
  * with group size (num_q_heads / kv_heads) <= 16.  Page ids outside
  * [0, num_pages) or out-of-range lengths raise KVQ_ERR_DEVICE_RANGE in the

@@ -44,6 +44,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -486,6 +487,10 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
 #pragma unroll
       for (int i = 0; i < 16; ++i) w16[i] = 0u;
     }
+    if (a.neg_q) {  // sm_scale < 0: negate the query (bf16 sign bits), scale by |sm_scale|
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w16[i] ^= 0x80008000u;
+    }
     if constexpr (QF8) {
       // FP8-domain attention: E4M3 codes of q / q_scale (the query quantization
       // rule of the store), the B operand of the m16n8k32 FP8 MMAs
@@ -740,8 +745,9 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
         x0 = fmaxf(x0, fmaxf(sc[tt][0], sc[tt][2]));
         x1 = fmaxf(x1, fmaxf(sc[tt][1], sc[tt][3]));
       }
-      x0 *= c0;
-      x1 *= c1;
+      // scale (c >= 0); an all-masked chunk keeps -inf (its p are set to 0 below)
+      x0 = (x0 == -INFINITY) ? x0 : x0 * c0;
+      x1 = (x1 == -INFINITY) ? x1 : x1 * c1;
       if (__any_sync(0xffffffffu, x0 > m0 + kLazy || x1 > m1 + kLazy)) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -766,8 +772,12 @@ __device__ void segment(const DecodeArgs& a, Ring& ring, int w, int b, int h, in
       // ---- O^T += V^T P^T ----
 #pragma unroll
       for (int tt = 0; tt < NT; ++tt) {
-        const float p0 = ex2(fmaf(sc[tt][0], c0, -m0)), p1 = ex2(fmaf(sc[tt][1], c1, -m1));
-        const float p2 = ex2(fmaf(sc[tt][2], c0, -m0)), p3 = ex2(fmaf(sc[tt][3], c1, -m1));
+        float p0 = ex2(fmaf(sc[tt][0], c0, -m0)), p1 = ex2(fmaf(sc[tt][1], c1, -m1));
+        float p2 = ex2(fmaf(sc[tt][2], c0, -m0)), p3 = ex2(fmaf(sc[tt][3], c1, -m1));
+        if (!FULL && nvalid[tt] < kTile) {  // masked tokens: 0 whatever the scale (c = 0 included)
+          if (r >= nvalid[tt]) p0 = p1 = 0.f;
+          if (r + 8 >= nvalid[tt]) p2 = p3 = 0.f;
+        }
         l0 += p0 + p2;
         l1 += p1 + p3;
         const uint8_t* tb = stage + tt * Tr::kTileBytes;
@@ -1097,7 +1107,10 @@ cudaError_t launch_decode(const Geometry& g, const LayerView& L, const DecodePla
   // per-head scales multiply in the kernel, after the same sm_scale * log2(e)
   a.kfac = hs.scale[0];
   a.vfac = hs.scale[1];
-  a.qscale = sm_scale * 1.4426950408889634f * (a.kfac ? 1.0f : k_factor);
+  // the softmax runs on positive logit scales: a negative sm_scale is folded
+  // into the query's sign (exact)
+  a.neg_q = sm_scale < 0.f;
+  a.qscale = std::fabs(sm_scale) * 1.4426950408889634f * (a.kfac ? 1.0f : k_factor);
   a.v_factor = v_factor;
   a.pt_rows = pt_rows;
   a.pt_nrows = pt_nrows;

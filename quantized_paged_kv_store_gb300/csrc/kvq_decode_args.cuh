@@ -35,6 +35,7 @@ struct DecodeArgs {
   const int32_t* pt_rows;  // extend: page-table row of each query token b (or null: row b)
   int pt_nrows;            // rows of the page table when pt_rows is set
   int fault_wait;          // failure-detection test: each warp's first stage wait runs out
+  int neg_q;               // sm_scale < 0: the query enters negated and qscale holds |sm_scale|
   int nqs;                 // FP8-domain attention: 1 (per tensor) or Hq q scales in qsc
   float qsc[kMaxQScales];  // FP8-domain attention: q_scale per tensor / per q head
 };

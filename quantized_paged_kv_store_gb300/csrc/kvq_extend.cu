@@ -22,8 +22,9 @@
 //     global scale stays out and is applied to the logits and the output);
 //   - one thread issues S = Q K^T (M = 128 rows, N = 64 tokens, K = 128 in
 //     eight tcgen05.mma kind::f16 steps, fp32 accumulators in tensor memory;
-//     Q in f16 is scaled per row by a power of two that keeps it exact) and
-//     commits to an mbarrier;
+//     A = Q from tensor memory, where each thread stored its row once, so the
+//     tensor cores read only K from shared memory; Q in f16 is scaled per row
+//     by a power of two that keeps it exact) and commits to an mbarrier;
 //   - each thread loads its row of S from tensor memory, runs the online
 //     softmax (base 2, lazy rescale when its maximum grows by more than 2^8,
 //     causal mask by q_len) and stores P back to tensor memory in f16 (or, for
@@ -53,14 +54,16 @@ constexpr uint32_t kXWaitLimit = 1u << 22;
 
 // tensor-memory columns: up to four S slots (64 fp32 columns each; P of a
 // chunk is written back over its own S slot: f16 in 32 columns, or bf16 high
-// and low parts in 64) and O (128 fp32 columns, two halves of head_dim)
+// and low parts in 64), O (128 fp32 columns, two halves of head_dim) and Q
+// (64 columns of f16 / bf16 pairs, the A operand of Q K^T)
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 64 * kMaxSlots;
+constexpr uint32_t kColQ = kColO + 128;
 constexpr uint32_t kTmemCols = 512;
+static_assert(kColQ + 64 <= kTmemCols, "tensor-memory columns");
 
 // shared memory (dynamic, 1024-byte aligned offsets)
-constexpr int kSQ = 0;                              // Q: 2 K-atoms x 128 rows x 128 B
-constexpr int kSKV = kSQ + 2 * kXRows * 128;        // slots of [K tile | V tile]
+constexpr int kSKV = 0;                             // slots of [K tile | V tile]
 constexpr int kTileKV = 2 * kChunk * 128;           // one K (or V) tile: 2 atoms x 64 tokens x 128 B
 
 template <kvq_format F>
@@ -94,7 +97,8 @@ struct ExtendArgs {
   const uint8_t* vs;
   int n, S, max_pages, H, Hq, G, P;
   long long num_pages;
-  float qscale;              // sm_scale * log2(e) * per-tensor K factor (without it if kfac)
+  float qscale;              // |sm_scale| * log2(e) * per-tensor K factor (without it if kfac)
+  int neg_q;                 // sm_scale < 0: the query enters negated
   float v_factor;
   const float* kfac;         // per-kv-head K / V scales, or null
   const float* vfac;
@@ -156,10 +160,6 @@ __host__ __device__ constexpr uint32_t idesc_16(uint32_t bf, uint32_t n, uint32_
   return (1u << 4) | (bf << 7) | (bf << 10) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
-               :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
                :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
@@ -212,6 +212,18 @@ __device__ __forceinline__ float ex2x(float x) {
 // Offset of 16-byte chunk c (0..7) of row `row` in a 128B-swizzled atom.
 __device__ __forceinline__ uint32_t sw_off(int row, int c) { return (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4)); }
 
+// Raw stage layout of one K (or V) data region: 16-byte piece p of the half
+// row (token tt, half hf) sits at natural index n = tt * kRow / 16 + hf * kRow
+// / 32 + p, with the low three bits of n XORed by tt & 7 -- a permutation
+// inside every 128-byte line, so that eight consecutive tokens (a quarter
+// warp of dequant threads) read eight different bank groups.
+template <kvq_format F>
+__device__ __forceinline__ uint32_t raw_off(int tt, int hf, int p) {
+  using Tr = XTraits<F>;
+  const uint32_t n = (uint32_t)(tt * (Tr::kRow / 16) + hf * (Tr::kRow / 32) + p);
+  return (n ^ (uint32_t)(tt & 7)) << 4;
+}
+
 // Dequantizes half a token row (64 head_dim elements, half hf) of K or V from
 // the raw stage into 32 packed pairs -- f16x2 for the FP8 and NVFP4 caches,
 // bf16x2 for the others -- exactly; the per-tensor / global scale is not
@@ -220,17 +232,17 @@ template <kvq_format F>
 __device__ __forceinline__ void dequant_half(const uint8_t* data, const uint8_t* scl, int tt, int hf,
                                              uint32_t (&o)[32]) {
   using Tr = XTraits<F>;
-  const uint8_t* row = data + tt * Tr::kRow + hf * (Tr::kRow / 2);
+  auto piece = [&](int p) { return *reinterpret_cast<const uint4*>(data + raw_off<F>(tt, hf, p)); };
   if (F == KVQ_BF16) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const uint4 v = reinterpret_cast<const uint4*>(row)[c];
+      const uint4 v = piece(c);
       o[4 * c] = v.x; o[4 * c + 1] = v.y; o[4 * c + 2] = v.z; o[4 * c + 3] = v.w;
     }
   } else if (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const uint4 v = reinterpret_cast<const uint4*>(row)[c];
+      const uint4 v = piece(c);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -240,7 +252,7 @@ __device__ __forceinline__ void dequant_half(const uint8_t* data, const uint8_t*
       }
     }
   } else {
-    const uint4 v0 = reinterpret_cast<const uint4*>(row)[0], v1 = reinterpret_cast<const uint4*>(row)[1];
+    const uint4 v0 = piece(0), v1 = piece(1);
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scl + tt * 8 + hf * 4);
 #pragma unroll
@@ -301,6 +313,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   const bool qvalid = qi < a.n;
   const int qhead = h * a.G + (int)(R % a.G);
   float qmul = 1.f;
+  uint4 qv[16];  // this thread's Q row (row warps), stored to tensor memory below
   if (!producer) {
     int s = -1, T = 0;
     if (qvalid) {
@@ -313,14 +326,17 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
     }
     row_seq[rho] = s;
     row_len[rho] = T;
-    // Q row -> 128B-swizzled K-major tile (two 64-element K atoms); for the
-    // f16 operand formats the row is scaled by 2^-sq so that its largest
-    // magnitude lies in [2^14, 2^15) and every bf16 value of it is exact in
-    // f16 (2^sq joins the row's logit scale)
+    // Q row as 64 pairs (d, d + 1); for the f16 operand formats the row is
+    // scaled by 2^-sq so that its largest magnitude lies in [2^14, 2^15) and
+    // every bf16 value of it is exact in f16 (2^sq joins the row's logit scale)
     const uint4* src = reinterpret_cast<const uint4*>(a.q + ((qvalid ? qi : 0) * a.Hq + qhead) * kHeadDim);
-    uint4 qv[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) qv[c] = qvalid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    if (a.neg_q) {  // sm_scale < 0: negate the query (bf16 sign bits), scale by |sm_scale|
+      const uint32_t f = 0x80008000u;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) qv[c] = make_uint4(qv[c].x ^ f, qv[c].y ^ f, qv[c].z ^ f, qv[c].w ^ f);
+    }
     if constexpr (Tr::kF16) {
       uint32_t m2 = 0u;
 #pragma unroll
@@ -348,9 +364,6 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
         qv[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
       }
     }
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-      *reinterpret_cast<uint4*>(sm + kSQ + (c >> 3) * (kXRows * 128) + sw_off(rho, c & 7)) = qv[c];
   }
   if (tid == 0) {
     // K/V ready and P ready collect one arrival per dequant / row warp
@@ -374,6 +387,21 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lane quarter
+  // Q rows into tensor memory: lane = row, column 4c + i = pair i of qv[c]
+  if (!producer) {
+    uint32_t w0[32], w1[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      w0[4 * c] = qv[c].x; w0[4 * c + 1] = qv[c].y; w0[4 * c + 2] = qv[c].z; w0[4 * c + 3] = qv[c].w;
+      w1[4 * c] = qv[8 + c].x; w1[4 * c + 1] = qv[8 + c].y; w1[4 * c + 2] = qv[8 + c].z; w1[4 * c + 3] = qv[8 + c].w;
+    }
+    tmem_st32(tmem + lane_off + kColQ, w0);
+    tmem_st32(tmem + lane_off + kColQ + 32, w1);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   const float cs = (a.kfac ? a.qscale * __ldg(a.kfac + h) : a.qscale) * qmul;
   const float vf = a.vfac ? __ldg(a.vfac + h) : a.v_factor;
@@ -450,9 +478,8 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
           const uint32_t kb = sm_u32 + kSKV + slot * 2 * kTileKV;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint64_t ad = sw128_desc(sm_u32 + kSQ + (j >> 2) * (kXRows * 128) + (j & 3) * 32, 1024);
             const uint64_t bd = sw128_desc(kb + (j >> 2) * (kChunk * 128) + (j & 3) * 32, 1024);
-            mma_ss(tmem + kColS + 64 * slot, ad, bd, kIdQK, j > 0);
+            mma_ts(tmem + kColS + 64 * slot, tmem + kColQ + 8 * j, bd, kIdQK, j > 0);
           }
           mma_commit(bar_s + 8 * slot);
         }
@@ -471,7 +498,10 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
       // stage with cp.async, kRaw chunks ahead, and is the only thread that
       // reads that slice back; a stage's mbarrier completes once all 128
       // threads' copies have landed.  Absent tokens and bad pages zero-fill.
-      const int ptid = tid - 128, tt = ptid >> 1, hf = ptid & 1;
+      // A warp holds 16 consecutive tokens x both halves (lanes 0-15 half 0),
+      // so a quarter warp writes eight tokens' rows of one swizzled tile: no
+      // bank conflicts.
+      const int ptid = tid - 128, tt = ((ptid >> 5) << 4) | (ptid & 15), hf = (ptid >> 4) & 1;
       auto page_of = [&](int c) -> int {
         const int tok = c * kChunk + tt;
         return (c < c1 && tok < maxT) ? __ldg(prow + tok / a.P) : -1;
@@ -484,13 +514,13 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
         const long long rowi = ok ? ((long long)page * a.H + h) * a.P + tok % a.P : 0;
         const uint32_t stage = sm_u32 + kSRaw + st * Tr::kStage;
         constexpr int kHalf = Tr::kRow / 2;
-        const uint32_t dk = stage + tt * Tr::kRow + hf * kHalf;
         const uint8_t* sk = a.kd + rowi * Tr::kRow + hf * kHalf;
         const uint8_t* sv = a.vd + rowi * Tr::kRow + hf * kHalf;
 #pragma unroll
         for (int i = 0; i < kHalf / 16; ++i) {
-          cp_async16z(dk + 16 * i, sk + 16 * i, ok);
-          cp_async16z(dk + Tr::kData + 16 * i, sv + 16 * i, ok);
+          const uint32_t dk = stage + raw_off<F>(tt, hf, i);
+          cp_async16z(dk, sk + 16 * i, ok);
+          cp_async16z(dk + Tr::kData, sv + 16 * i, ok);
         }
         if constexpr (Tr::kScales) {
           const uint32_t ds = stage + 2 * Tr::kData + tt * 8 + hf * 4;
@@ -839,7 +869,10 @@ cudaError_t launch_extend(const Geometry& g, const LayerView& L, const void* q, 
   a.num_pages = g.num_pages;
   a.kfac = hs.scale[0];
   a.vfac = hs.scale[1];
-  a.qscale = sm_scale * 1.4426950408889634f * (a.kfac ? 1.0f : k_factor);
+  // the softmax runs on positive logit scales: a negative sm_scale is folded
+  // into the query's sign (exact)
+  a.neg_q = sm_scale < 0.f;
+  a.qscale = std::fabs(sm_scale) * 1.4426950408889634f * (a.kfac ? 1.0f : k_factor);
   a.v_factor = v_factor;
   a.err = err;
   a.splits = std::max(1, splits);

@@ -239,3 +239,35 @@ def test_decode_whole_stages_per_worker(kvq, orc, cuda, fmt, L, P):
     wl = synth.make_workload(f"w_{fmt}", fmt, Hq=8, Hkv=1, P=P, seq_lens=[L] * 8, seed=L + P)
     got, ref = _run(kvq, orc, wl)
     assert_attention_close(got, ref, f"{fmt} L={L} P={P}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("sm_scale", [-0.0884, 0.0, -1.5])
+def test_decode_nonpositive_sm_scale(kvq, orc, cuda, fmt, sm_scale):
+    """sm_scale is any finite number: zero gives the mean of V, a negative one
+    favours the least similar keys (the kernel folds the sign into the query)."""
+    wl = synth.make_workload(f"neg_{fmt}", fmt, Hq=16, Hkv=4, seq_lens=[70, 1, 33, 200], seed=93)
+    wl.sm_scale = sm_scale
+    got, ref = _run(kvq, orc, wl)
+    assert_attention_close(got, ref, f"{fmt} sm_scale={sm_scale}")
+
+
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "fp8_e5m2"])
+def test_decode_fp8q_negative_sm_scale(kvq, orc, cuda, fmt):
+    """FP8-domain decode with sm_scale < 0 against the oracle's attention over
+    the dequantized query."""
+    wl = synth.make_workload(f"negq_{fmt}", fmt, Hq=16, Hkv=4, seq_lens=[70, 1, 33, 200], seed=94)
+    wl.sm_scale = -0.0884
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    qs = [float(wl.q_scales(0)[0])]
+    out = c.decode_attention_fp8q(0, bits_to_cuda(wl.q(0)), qs, torch.from_numpy(wl.page_table).cuda(),
+                                  torch.from_numpy(wl.seq_lens).cuda(), wl.sm_scale)
+    torch.cuda.synchronize()
+    assert c.device_error() == 0
+    got = synth.bf16_bits_to_float(
+        out.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+    oc = oracle_cache_for(orc, wl, 0)
+    ref, rc = oc.decode_attention_fp8q(wl.q(0), qs, wl.page_table, wl.seq_lens, wl.sm_scale)
+    assert rc == 0
+    assert_attention_close(got, ref, f"{fmt} fp8 query, sm_scale < 0")

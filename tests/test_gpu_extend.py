@@ -130,3 +130,20 @@ def test_extend_split_and_unsplit_plans_agree(kvq, orc, cuda, fmt):
         got = synth.bf16_bits_to_float(cuda_to_bits(out)).astype(np.float64)
         assert_attention_close(got, ref, f"{fmt} extend workspace {ws_bytes}")
         outs.append(got)
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("sm_scale", [-0.0884, 0.0])
+def test_extend_nonpositive_sm_scale(kvq, orc, cuda, fmt, sm_scale):
+    """sm_scale is any finite number (zero: the mean of V over the prefix; a
+    negative one: the kernel folds the sign into the query)."""
+    wl = synth.make_workload(f"extneg_{fmt}", fmt, Hq=16, Hkv=4, seq_lens=[300, 65, 130, 17], seed=32)
+    wl.sm_scale = sm_scale
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    q, q_seq, q_len = _queries(wl, [24, 1, 16, 17], seed=3)
+    got = _gpu_extend(c, wl, q, q_seq, q_len)
+    assert c.device_error() == 0
+    ref, rc = oracle_cache_for(orc, wl).extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
+    assert rc == 0
+    assert_attention_close(got, ref, f"{fmt} extend sm_scale={sm_scale}")

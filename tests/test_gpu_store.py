@@ -192,3 +192,46 @@ def test_fp4_store_every_bf16_value(kvq, orc, cuda, fmt, g):
     oc = orc.OracleCache(fmt, 1, D, P, num_pages)
     assert oc.quantize_store(x, x[::-1].copy(), slots, scales) == 0
     _assert_pools_equal(gpu_pools(c, 0), oc, fmt)
+
+
+def _bf16_neighbors(v):
+    """bf16 bit patterns of v and of its two bf16 neighbours (v exactly representable)."""
+    b = int(np.array([v], dtype=np.float32).view(np.uint32)[0] >> 16)
+    return [b - 1, b, b + 1]
+
+
+@pytest.mark.parametrize("g", [1.0, 1.0 + 2.0 ** -22, 1.0 - 2.0 ** -23, 1.0 + 2.0 ** -20, 1.0 - 2.0 ** -19,
+                               0.75 * (1.0 + 2.0 ** -21)])
+def test_nvfp4_store_near_decision_points(kvq, orc, cuda, g):
+    """Blocks whose quotients x / S fall on, or within a few ulp of, the E2M1
+    decision points 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 (and the code values):
+    each block holds 6 * 2^k, so its scale code decodes to 2^k and S = 2^k g;
+    g = 1 gives exact ties, g = 1 -+ 2^-22.. puts x / S just above / below them.
+    Every code must be the correctly rounded quotient's, byte for byte with the
+    oracle ("SGLang PR #21954 analysis: NVFP4 KV cache", NVFP4 two-level scaling)."""
+    D, P = 128, 16
+    pts = [0.25, 0.5, 0.75, 1.0, 1.25, 1.5, 1.75, 2.0, 2.5, 3.0, 3.5, 4.0, 5.0]
+    cand = []
+    for m in pts:
+        for b in _bf16_neighbors(m):
+            cand += [b, b | 0x8000]
+    rows = []
+    for k in (0, -3, 5):
+        six = int(np.array([6.0 * 2.0 ** k], dtype=np.float32).view(np.uint32)[0] >> 16)
+        sc = [((b & 0x7FFF) + (k << 7)) | (b & 0x8000) for b in cand]  # times 2^k (exponent add)
+        blocks = [[six] + sc[i:i + 15] for i in range(0, len(sc), 15)]
+        blocks = [bl + [0] * (16 - len(bl)) for bl in blocks]
+        flat = [x for bl in blocks for x in bl]
+        flat += [0] * (-len(flat) % D)
+        rows += [flat[i:i + D] for i in range(0, len(flat), D)]
+    x = np.array(rows, dtype=np.uint16).reshape(len(rows), 1, D)
+    n = x.shape[0]
+    num_pages = (n + P - 1) // P
+    slots = np.arange(n, dtype=np.int64)
+    scales = [g, 2.0 * g]
+    c = kvq.KVQCache("nvfp4", 1, 1, D, P, num_pages)
+    c.quantize_and_store(0, bits_to_cuda(x), bits_to_cuda(x[::-1].copy()), torch.from_numpy(slots).cuda(),
+                         scales)
+    oc = orc.OracleCache("nvfp4", 1, D, P, num_pages)
+    assert oc.quantize_store(x, x[::-1].copy(), slots, scales) == 0
+    _assert_pools_equal(gpu_pools(c, 0), oc, "nvfp4")
