@@ -356,9 +356,11 @@ PER_FORMAT = ("nvfp4", "fp4_mx_block16", "fp8_e4m3", "fp8_e5m2", "bf16")
 
 def per_format_cells(args, wl, ks, vs, d_q, d_pt, d_sl, exact, dev, peak):
     """Decode attention of the same workload (same K/V draws, every token
-    stored) in each cache format: mean CUDA-event time per call, algorithmic
-    GB/s and fraction of peak, and the quantization error of its output on the
-    sampled sequences."""
+    stored) in each cache format: mean CUDA-event time per call issued from
+    Python, the device time per call from CUDA-graph replay (the way a serving
+    loop replays decode; no host launch gaps), algorithmic GB/s and fraction of
+    peak of each, and the quantization error of its output on the sampled
+    sequences."""
     import numpy as np
     import torch
     import quantized_paged_kv_store_gb300 as kvq
@@ -378,9 +380,16 @@ def per_format_cells(args, wl, ks, vs, d_q, d_pt, d_sl, exact, dev, peak):
                          steps, warm)
         if cache.device_error() != 0:
             raise RuntimeError(f"device error in the {f} per-format decode")
+        gus = _graph_us(lambda st: cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale, out, ws,
+                                                          stream=st))
+        if cache.device_error() != 0:
+            raise RuntimeError(f"device error in the {f} per-format decode (graph)")
         nbytes = algorithmic_bytes(wl, f)
         gbs = nbytes / (ms * 1e-3) / 1e9
+        ggbs = nbytes / (gus * 1e-6) / 1e9
         cells[f] = {"ms_per_call": round(ms, 5), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                    "graph_ms_per_call": round(gus * 1e-3, 5), "graph_GBps": round(ggbs, 1),
+                    "graph_frac": round(ggbs / peak, 4),
                     "bytes_per_call": nbytes, "calls": steps,
                     "quant_error": {k: (round(v, 6) if isinstance(v, float) else v)
                                     for k, v in quant_error(out_rows(out, exact.keys()), exact).items()}}
@@ -390,11 +399,16 @@ def per_format_cells(args, wl, ks, vs, d_q, d_pt, d_sl, exact, dev, peak):
             qs = [float(x) for x in wl.q_scales(0)]
             ms = _time_calls(lambda: cache.decode_attention_fp8q(0, d_q, qs, d_pt, d_sl, wl.sm_scale,
                                                                  out, ws), steps, warm)
+            gus = _graph_us(lambda st: cache.decode_attention_fp8q(0, d_q, qs, d_pt, d_sl, wl.sm_scale,
+                                                                   out, ws, stream=st))
             if cache.device_error() != 0:
                 raise RuntimeError(f"device error in the {f} FP8-query decode")
             gbs = nbytes / (ms * 1e-3) / 1e9
+            ggbs = nbytes / (gus * 1e-6) / 1e9
             cells[f + "+fp8_query"] = {
                 "ms_per_call": round(ms, 5), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                "graph_ms_per_call": round(gus * 1e-3, 5), "graph_GBps": round(ggbs, 1),
+                "graph_frac": round(ggbs / peak, 4),
                 "bytes_per_call": nbytes, "calls": steps, "q_scale": qs[0],
                 "quant_error": {k: (round(v, 6) if isinstance(v, float) else v)
                                 for k, v in quant_error(out_rows(out, exact.keys()), exact).items()}}
