@@ -143,11 +143,13 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand: start
-// address, leading / stride byte offsets (the stride is the distance between
-// 8-row groups), descriptor version 1 (bits 46-48), layout 2 = 128B swizzle.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t sbo) {
+// address, leading byte offset (MN-major operands: the distance between the
+// 64-element swizzle atoms along N; unused by K-major ones), stride byte
+// offset (the distance between 8-row groups along K), descriptor version 1
+// (bits 46-48), layout 2 = 128B swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t sbo, uint32_t lbo = 16) {
   uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)1 << 16;  // leading byte offset 16 (unused by these layouts)
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   const float vf = a.vfac ? __ldg(a.vfac + h) : a.v_factor;
   constexpr uint32_t kBf = Tr::kF16 ? 0u : 1u;
   constexpr uint32_t kIdQK = idesc_16(kBf, kChunk, kXRows, 0);
-  constexpr uint32_t kIdPV = idesc_16(kBf, 64, kXRows, 1);
+  constexpr uint32_t kIdPV = idesc_16(kBf, kHeadDim, kXRows, 1);  // N = all of head_dim
 
   // chunk counters over the CTA's life: chunk number k uses raw stage
   // k % kRaw and K/V and S slot k % kSlots, with mbarrier phase parity
@@ -449,15 +451,13 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
         if (lane == 0) {
           const uint32_t pcol = tmem + kColS + 64 * slot;
           const uint32_t vbase = sm_u32 + kSKV + slot * 2 * kTileKV + kTileKV;
+          // one MMA per 16 tokens covers both 64-element halves of head_dim
+          // (B atoms kChunk * 128 bytes apart along N)
 #pragma unroll
           for (int j = 0; j < kChunk / 16; ++j) {
-#pragma unroll
-            for (int nh = 0; nh < 2; ++nh) {
-              const uint64_t bd = sw128_desc(vbase + nh * (kChunk * 128) + j * 2048, 1024);
-              const uint32_t d = tmem + kColO + 64 * nh;
-              mma_ts(d, pcol + 8 * j, bd, kIdPV, (start && j == 0) ? 0u : 1u);
-              if (!Tr::kF16) mma_ts(d, pcol + 32 + 8 * j, bd, kIdPV, 1u);
-            }
+            const uint64_t bd = sw128_desc(vbase + j * 2048, 1024, kChunk * 128);
+            mma_ts(tmem + kColO, pcol + 8 * j, bd, kIdPV, (start && j == 0) ? 0u : 1u);
+            if (!Tr::kF16) mma_ts(tmem + kColO, pcol + 32 + 8 * j, bd, kIdPV, 1u);
           }
           mma_commit(bar_o + 8 * slot);
         }
