@@ -147,3 +147,19 @@ def test_extend_nonpositive_sm_scale(kvq, orc, cuda, fmt, sm_scale):
     ref, rc = oracle_cache_for(orc, wl).extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
     assert rc == 0
     assert_attention_close(got, ref, f"{fmt} extend sm_scale={sm_scale}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8_e5m2", "nvfp4", "fp4_mx_block16"])
+@pytest.mark.parametrize("P", [32, 48])
+def test_extend_page_sizes(kvq, orc, cuda, fmt, P):
+    """Pages of 32 and 48 tokens: a 64-token chunk spans pages at other
+    boundaries (48: not a power of two)."""
+    wl = synth.make_workload(f"extP_{fmt}", fmt, Hq=16, Hkv=4, P=P, seq_lens=[300, 65, 130, 17], seed=33 + P)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    q, q_seq, q_len = _queries(wl, [24, 1, 16, 17], seed=4)
+    got = _gpu_extend(c, wl, q, q_seq, q_len)
+    assert c.device_error() == 0
+    ref, rc = oracle_cache_for(orc, wl).extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
+    assert rc == 0
+    assert_attention_close(got, ref, f"{fmt} extend P={P}")
