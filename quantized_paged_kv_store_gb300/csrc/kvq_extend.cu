@@ -78,9 +78,10 @@ struct XTraits {
   static constexpr int kData = kChunk * kRow;
   static constexpr int kScl = kScales ? kChunk * 8 : 0;
   static constexpr int kStage = 2 * kData + 2 * kScl;
-  // K/V and S slots and raw stages in flight: as many as shared memory holds
+  // K/V and S slots in flight: as many as shared memory holds; raw stages:
+  // four (more copies in flight per thread made the copy issue slower)
   static constexpr int kSlots = (F == KVQ_BF16) ? 3 : 4;
-  static constexpr int kRaw = (F == KVQ_BF16) ? 3 : (F == KVQ_FP8_E4M3 || F == KVQ_FP8_E5M2) ? 4 : 6;
+  static constexpr int kRaw = (F == KVQ_BF16) ? 3 : 4;
   static constexpr int kSRaw = kSKV + kSlots * 2 * kTileKV;  // raw stages
   static constexpr int kSmem = kSRaw + kRaw * kStage + 1024;  // + alignment slack
 };
