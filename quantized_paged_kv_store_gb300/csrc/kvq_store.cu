@@ -37,6 +37,9 @@ struct StoreArgs {
   int nb_shift;          // log2(nb) if nb is a power of two, else -1
   int p_shift;           // log2(P) if P is a power of two, else -1
   int hb;                // H * nb: blocks per token
+  int ib;                // items per token: hb / blocks per item
+  int nbi;               // items per row: nb / blocks per item
+  int nbi_shift;         // log2(nbi) if nbi is a power of two, else -1
   bool fast_div;         // scales in [2^-80, 2^80]: reciprocal-based division is exact
   int64_t num_pages;
   int* err;
@@ -212,7 +215,10 @@ __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t 
 // while it computes.  PH: the scale of each item's kv head comes from the
 // per-head arrays ("Quantized KV cache" (vLLM), Supported schemes:
 // per-attention-head scales) instead of the per-tensor launch argument.
-template <kvq_format F, bool PH>
+// BPI (blocks per item): the FP4 stores take two adjacent blocks of a row per
+// item, so that the slot, page and row arithmetic and the loop bookkeeping are
+// shared by both.
+template <kvq_format F, bool PH, int BPI>
 __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
   const int kv = blockIdx.y;
   // NVFP4 with a per-tensor global scale: the CTA's block-scale table
@@ -231,11 +237,11 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
   }
   // the item index advances by a constant stride, split once into (tokens, blocks)
   const long long S = (long long)gridDim.x * blockDim.x;
-  const long long S_tok = S / a.hb;
-  const int S_pair = (int)(S - S_tok * a.hb);
+  const long long S_tok = S / a.ib;
+  const int S_pair = (int)(S - S_tok * a.ib);
   const long long it0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  long long tok = it0 / a.hb;
-  int pair = (int)(it0 - tok * a.hb);
+  long long tok = it0 / a.ib;
+  int pair = (int)(it0 - tok * a.ib);  // item of the token: blocks BPI pair ..
   if (tok >= a.n) return;
   // select per K/V without indexing the parameter arrays (that would copy them to local memory)
   const float s = kv ? a.s[1] : a.s[0], rs = kv ? a.rs[1] : a.rs[0];
@@ -244,30 +250,34 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
   uint8_t* const scl = kv ? a.scales[1] : a.scales[0];
   const float* const hsp = kv ? a.hs[1] : a.hs[0];
   const float* const hrp = kv ? a.hr[1] : a.hr[0];
-  const int64_t tok_elems = (int64_t)a.H * a.D;  // input row of one token; block `pair` at pair * 16
+  const int64_t tok_elems = (int64_t)a.H * a.D;  // input row of one token; item `pair` at pair * 16 BPI
   const int64_t capacity = a.num_pages * a.P;
 
-  const uint4* src = reinterpret_cast<const uint4*>(xin + tok * tok_elems + pair * 16);
-  uint4 c0 = __ldg(src), c1 = __ldg(src + 1);
+  const uint4* src = reinterpret_cast<const uint4*>(xin + tok * tok_elems + pair * (16 * BPI));
+  uint4 c[2 * BPI];
+#pragma unroll
+  for (int i = 0; i < 2 * BPI; ++i) c[i] = __ldg(src + i);
   int64_t slot = __ldg(a.slots + tok);
   for (;;) {
     long long ntok = tok + S_tok;
     int npair = pair + S_pair;
-    if (npair >= a.hb) {
-      npair -= a.hb;
+    if (npair >= a.ib) {
+      npair -= a.ib;
       ++ntok;
     }
     const bool more = ntok < a.n;
-    uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
+    uint4 n[2 * BPI];
+#pragma unroll
+    for (int i = 0; i < 2 * BPI; ++i) n[i] = make_uint4(0, 0, 0, 0);
     int64_t nslot = -1;
     if (more) {
-      const uint4* ns = reinterpret_cast<const uint4*>(xin + ntok * tok_elems + npair * 16);
-      n0 = __ldg(ns);
-      n1 = __ldg(ns + 1);
+      const uint4* ns = reinterpret_cast<const uint4*>(xin + ntok * tok_elems + npair * (16 * BPI));
+#pragma unroll
+      for (int i = 0; i < 2 * BPI; ++i) n[i] = __ldg(ns + i);
       nslot = __ldg(a.slots + ntok);
     }
-    const int h = a.nb_shift >= 0 ? (pair >> a.nb_shift) : pair / a.nb;
-    const int blk = pair - h * a.nb;
+    const int h = a.nbi_shift >= 0 ? (pair >> a.nbi_shift) : pair / a.nbi;
+    const int blk = (pair - h * a.nbi) * BPI;  // first block of the item
     if (slot >= capacity) {
       if (blk == 0) atomicOr(a.err, kErrRange);
     } else if (slot >= 0) {
@@ -280,21 +290,25 @@ __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
         off = slot - page * a.P;
       }
       const int64_t r = (page * a.H + h) * a.P + off;  // destination row
-      if constexpr (PH) {
-        const float sh = __ldg(hsp + h), rh = __ldg(hrp + h);
-        store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, sh, rh, sh >= 0x1p-80f && sh <= 0x1p80f);
-      } else if constexpr (kTable) {
-        store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, s, rs, a.fast_div, tab,
-                       kv ? a.s6[1] : a.s6[0], kv ? a.rs6[1] : a.rs6[0]);
-      } else {
-        store_block<F>(dat, scl, r, blk, a.D, a.nb, c0, c1, s, rs, a.fast_div);
+#pragma unroll
+      for (int j = 0; j < BPI; ++j) {
+        if constexpr (PH) {
+          const float sh = __ldg(hsp + h), rh = __ldg(hrp + h);
+          store_block<F>(dat, scl, r, blk + j, a.D, a.nb, c[2 * j], c[2 * j + 1], sh, rh,
+                         sh >= 0x1p-80f && sh <= 0x1p80f);
+        } else if constexpr (kTable) {
+          store_block<F>(dat, scl, r, blk + j, a.D, a.nb, c[2 * j], c[2 * j + 1], s, rs, a.fast_div, tab,
+                         kv ? a.s6[1] : a.s6[0], kv ? a.rs6[1] : a.rs6[0]);
+        } else {
+          store_block<F>(dat, scl, r, blk + j, a.D, a.nb, c[2 * j], c[2 * j + 1], s, rs, a.fast_div);
+        }
       }
     }
     if (!more) break;
     tok = ntok;
     pair = npair;
-    c0 = n0;
-    c1 = n1;
+#pragma unroll
+    for (int i = 0; i < 2 * BPI; ++i) c[i] = n[i];
     slot = nslot;
   }
 }
@@ -401,26 +415,39 @@ int grid_for(int64_t items) {
 // more CTAs than there are items.  Measured on the 131072-token 70B-layer store:
 // one wave reaches 0.72 (bf16) to 0.89 (FP4 block-16) of the copy bandwidth,
 // four to eight waves 0.98 / 0.90, with the quantizing formats flat from four up.
-template <kvq_format F, bool PH>
-cudaError_t launch_store_as(const StoreArgs& a, int64_t items, cudaStream_t stream) {
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, store_kernel<F, PH>, 256, 0);
-  if (e != cudaSuccess) return e;
-  const int64_t wave = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) * 8 / 2);
-  const int64_t need = (items + 255) / 256;
-  dim3 grid((unsigned)std::min(wave, need), 2);
-  store_kernel<F, PH><<<grid, 256, 0, stream>>>(a);
-  return cudaGetLastError();
-}
-
 inline int log2_if_pow2(int v) {
   if (v <= 0 || (v & (v - 1))) return -1;
   int k = 0;
   while ((1 << k) < v) ++k;
   return k;
 }
+
+template <kvq_format F, bool PH, int BPI>
+cudaError_t launch_store_bpi(StoreArgs a, int64_t blocks, cudaStream_t stream) {
+  a.ib = a.hb / BPI;
+  a.nbi = a.nb / BPI;
+  a.nbi_shift = log2_if_pow2(a.nbi);
+  const int64_t items = blocks / BPI;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, store_kernel<F, PH, BPI>, 256, 0);
+  if (e != cudaSuccess) return e;
+  const int64_t wave = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) * 8 / 2);
+  const int64_t need = (items + 255) / 256;
+  dim3 grid((unsigned)std::min(wave, need), 2);
+  store_kernel<F, PH, BPI><<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// FP4 formats: two blocks per item when the row has an even block count
+template <kvq_format F, bool PH>
+cudaError_t launch_store_as(const StoreArgs& a, int64_t blocks, cudaStream_t stream) {
+  constexpr bool kFp4 = (F == KVQ_FP4_BLOCK16 || F == KVQ_NVFP4);
+  if (kFp4 && a.nb % 2 == 0) return launch_store_bpi<F, PH, kFp4 ? 2 : 1>(a, blocks, stream);
+  return launch_store_bpi<F, PH, 1>(a, blocks, stream);
+}
+
 
 cudaError_t launch_store(const Geometry& g, const LayerView& L, const void* k, const void* v,
                          const int64_t* slots, int num_tokens, float s_k, float s_v,
