@@ -418,10 +418,6 @@ int grid_for(int64_t items) {
 
 }  // namespace
 
-// Eight resident waves' worth of store CTAs (K and V halves together), never
-// more CTAs than there are items.  Measured on the 131072-token 70B-layer store:
-// one wave reaches 0.72 (bf16) to 0.89 (FP4 block-16) of the copy bandwidth,
-// four to eight waves 0.98 / 0.90, with the quantizing formats flat from four up.
 inline int log2_if_pow2(int v) {
   if (v <= 0 || (v & (v - 1))) return -1;
   int k = 0;
@@ -429,6 +425,11 @@ inline int log2_if_pow2(int v) {
   return k;
 }
 
+// Resident waves' worth of store CTAs (K and V halves together), never more
+// CTAs than there are items: eight for bf16 and FP8 (bf16 at one wave reaches
+// 0.72 of the copy bandwidth, at eight 0.97; FP8 at four 0.956, at eight
+// 0.998), four for the FP4 formats (NVFP4 at sixteen 0.760, eight 0.798, four
+// 0.810, two 0.802).
 template <kvq_format F, bool PH, int BPI>
 cudaError_t launch_store_bpi(StoreArgs a, int64_t blocks, cudaStream_t stream) {
   a.ib = a.hb / BPI;
@@ -440,19 +441,22 @@ cudaError_t launch_store_bpi(StoreArgs a, int64_t blocks, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, store_kernel<F, PH, BPI>, 256, 0);
   if (e != cudaSuccess) return e;
-  const int64_t wave = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) * 8 / 2);
+  constexpr int kWaves = (F == KVQ_FP4_BLOCK16 || F == KVQ_NVFP4) ? 4 : 8;
+  const int64_t wave = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) * kWaves / 2);
   const int64_t need = (items + 255) / 256;
   dim3 grid((unsigned)std::min(wave, need), 2);
   store_kernel<F, PH, BPI><<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
-// FP4 formats: two blocks per item when the row has an even block count
-// (measured: NVFP4 0.725 -> 0.798 of the copy bandwidth, FP4 block-16 0.867 -> 0.978)
+// The quantizing formats: two blocks per item when the row has an even block
+// count (measured on the 131072-token store: NVFP4 0.725 -> 0.811 of the copy
+// bandwidth, FP4 block-16 0.867 -> 0.987, FP8 0.950 -> 0.998, with the
+// grid sizes above)
 template <kvq_format F, bool PH>
 cudaError_t launch_store_as(const StoreArgs& a, int64_t blocks, cudaStream_t stream) {
-  constexpr bool kFp4 = (F == KVQ_FP4_BLOCK16 || F == KVQ_NVFP4);
-  if (kFp4 && a.nb % 2 == 0) return launch_store_bpi<F, PH, kFp4 ? 2 : 1>(a, blocks, stream);
+  constexpr bool kPair = (F != KVQ_BF16);
+  if (kPair && a.nb % 2 == 0) return launch_store_bpi<F, PH, kPair ? 2 : 1>(a, blocks, stream);
   return launch_store_bpi<F, PH, 1>(a, blocks, stream);
 }
 
