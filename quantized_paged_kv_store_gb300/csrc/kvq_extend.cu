@@ -13,14 +13,15 @@
 // heads per kv head) -- one row per thread and per tensor-memory lane -- and
 // one split of the context (gridDim.z splits; their partial outputs and
 // log-sum-exps are merged by extend_merge_kernel).  Per 64-token chunk:
-//   - the dequant warps copy the raw K/V rows (and block scales) of the
-//     chunk into a ring of raw stages several chunks ahead with cp.async,
-//     each thread its own slice, completing on the stage's mbarrier;
-//   - every thread dequantizes half a token row of K and of V into f16 (FP8,
+//   - two copy warps copy the raw K/V rows (and block scales) of the chunk
+//     into a ring of raw stages several chunks ahead with cp.async,
+//     completing on the stage's mbarrier, and refill a stage once the
+//     dequant warps have read it;
+//   - every dequant thread dequantizes half a token row of K and of V into f16 (FP8,
 //     NVFP4) or bf16 (bf16, FP4 block-16) tiles in the 128-byte-swizzled
 //     layout the tensor cores read (exact for every format: the per-tensor /
 //     global scale stays out and is applied to the logits and the output);
-//   - one thread issues S = Q K^T (M = 128 rows, N = 64 tokens, K = 128 in
+//   - one elected thread of the MMA warp issues S = Q K^T (M = 128 rows, N = 64 tokens, K = 128 in
 //     eight tcgen05.mma kind::f16 steps, fp32 accumulators in tensor memory;
 //     A = Q from tensor memory, where each thread stored its row once, so the
 //     tensor cores read only K from shared memory; Q in f16 is scaled per row
@@ -46,7 +47,8 @@ namespace kvq {
 namespace {
 
 constexpr int kXRows = 128;        // (query, q head) rows per CTA = TMEM lanes
-constexpr int kXThreads = 288;     // warps 0-3: rows; 4-7: dequant; 8: MMA issue
+constexpr int kXThreads = 352;     // warps 0-3: rows; 4-7: dequant; 8: MMA issue; 9-10: copies
+constexpr int kCopyBase = 288;     // first copy thread
 constexpr int kMaxSlots = 4;       // K/V tiles and S slots in flight (per format below)
 constexpr int kChunk = 64;         // tokens per chunk (four 16-token tiles)
 constexpr int kMaxSplits = 16;
@@ -135,10 +137,6 @@ __device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, bool 
 __device__ __forceinline__ void cp_async4z(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
 }
-// Arrive on the mbarrier once every cp.async this thread issued has landed.
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -163,12 +161,17 @@ __host__ __device__ constexpr uint32_t idesc_16(uint32_t bf, uint32_t n, uint32_
   return (1u << 4) | (bf << 7) | (bf << 10) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// D (+)= A B with A in tensor memory, issued by one elected lane of a
+// converged warp (every lane passes the same, warp-uniform operands: issuing
+// from a lane-0 branch instead was 7% slower for the bf16-operand formats).
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+  asm volatile("{ .reg .pred e, p; elect.sync _|e, 0xffffffff; setp.ne.u32 p, %4, 0;\n"
+               "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
                :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+  asm volatile("{ .reg .pred e; elect.sync _|e, 0xffffffff;\n"
+               "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(bar) : "memory");
 }
 
 // 32 consecutive 32-bit tensor-memory columns of this thread's lane.
@@ -279,8 +282,8 @@ __device__ __forceinline__ void dequant_half(const uint8_t* data, const uint8_t*
   }
 }
 
-// Nine warps: three share one SM sub-partition's register file, so the
-// launch bound holds each thread to 168 registers.
+// Eleven warps: at most three share one SM sub-partition's register file, so
+// the launch bound holds each thread to 168 registers.
 template <kvq_format F>
 __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   using Tr = XTraits<F>;
@@ -290,15 +293,16 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   constexpr int kMaxRaw = 6;
   constexpr int kSlots = Tr::kSlots;
   constexpr int kSRaw = Tr::kSRaw;
-  __shared__ __align__(8) uint64_t bars[kMaxRaw + 4 * kMaxSlots];
+  __shared__ __align__(8) uint64_t bars[kMaxRaw + 4 * kMaxSlots + kMaxRaw];
   __shared__ uint32_t tmem_slot;
   __shared__ int row_seq[kXRows];
   __shared__ int row_len[kXRows];
   __shared__ int pass_seq, pass_max, pass_bad, dead;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool producer = warp >= 4;  // dequant warps 4-7 and the copy / MMA warp 8
+  const bool producer = warp >= 4;  // dequant warps 4-7, the MMA warp 8, copy warps 9-10
   const bool mma_warp = warp == 8;
+  const bool copy_warp = warp >= 9;
   const int h = blockIdx.y, split = blockIdx.z;
   const long long R0 = (long long)blockIdx.x * kXRows;
   const uint32_t base_u32 = smem_u32(xsm_raw);
@@ -308,6 +312,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
   const uint32_t bar_raw = smem_u32(&bars[0]), bar_kv = smem_u32(&bars[kMaxRaw]);
   const uint32_t bar_s = smem_u32(&bars[kMaxRaw + kMaxSlots]), bar_p = smem_u32(&bars[kMaxRaw + 2 * kMaxSlots]);
   const uint32_t bar_o = smem_u32(&bars[kMaxRaw + 3 * kMaxSlots]);
+  const uint32_t bar_rfree = smem_u32(&bars[kMaxRaw + 4 * kMaxSlots]);  // raw stage read by the dequant warps
 
   // ---- rows of this CTA (threads 0..127): (query, q head) = divmod(R0 + tid, G)
   const int rho = tid & (kXRows - 1);
@@ -369,13 +374,14 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
     }
   }
   if (tid == 0) {
-    // K/V ready and P ready collect one arrival per dequant / row warp
-    // raw stages: one arrival per dequant thread (its copies landed); K/V and
-    // P ready: one per dequant / row warp
+    // raw stage landed: one release arrival per copy warp (each copy thread
+    // adds a pending arrival that its copies complete); K/V and P ready: one
+    // per dequant / row warp; raw stage read: one per dequant warp
     for (int i = 0; i < kMaxRaw + 4 * kMaxSlots; ++i) {
       const int grp = i < kMaxRaw ? -1 : (i - kMaxRaw) / kMaxSlots;  // 0 K/V, 1 S, 2 P, 3 O
-      mbar_init(smem_u32(&bars[i]), grp < 0 ? 128 : (grp == 0 || grp == 2) ? 4 : 1);
+      mbar_init(smem_u32(&bars[i]), grp < 0 ? 2 : (grp == 0 || grp == 2) ? 4 : 1);
     }
+    for (int i = 0; i < kMaxRaw; ++i) mbar_init(smem_u32(&bars[kMaxRaw + 4 * kMaxSlots + i]), 4);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     dead = 0;
   }
@@ -443,22 +449,23 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
 
     if (mma_warp) {
       // ================= MMA warp: QK^T and PV issue ==========================
+      const uint32_t tmem_u = __shfl_sync(0xffffffffu, tmem, 0);  // warp-uniform operand base
       // O += P V of chunk number kk once its P is ready (acc == 0 starts the pass)
       auto issue_pv = [&](uint32_t kk, bool start) -> bool {
         const uint32_t slot = kk % kSlots;
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_p + 8 * slot, (kk / kSlots) & 1u));
         if (!ok) return false;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t pcol = tmem + kColS + 64 * slot;
+        {
+          const uint32_t pcol = tmem_u + kColS + 64 * slot;
           const uint32_t vbase = sm_u32 + kSKV + slot * 2 * kTileKV + kTileKV;
           // one MMA per 16 tokens covers both 64-element halves of head_dim
           // (B atoms kChunk * 128 bytes apart along N)
 #pragma unroll
           for (int j = 0; j < kChunk / 16; ++j) {
             const uint64_t bd = sw128_desc(vbase + j * 2048, 1024, kChunk * 128);
-            mma_ts(tmem + kColO, pcol + 8 * j, bd, kIdPV, (start && j == 0) ? 0u : 1u);
-            if (!Tr::kF16) mma_ts(tmem + kColO, pcol + 32 + 8 * j, bd, kIdPV, 1u);
+            mma_ts(tmem_u + kColO, pcol + 8 * j, bd, kIdPV, (start && j == 0) ? 0u : 1u);
+            if (!Tr::kF16) mma_ts(tmem_u + kColO, pcol + 32 + 8 * j, bd, kIdPV, 1u);
           }
           mma_commit(bar_o + 8 * slot);
         }
@@ -474,13 +481,13 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
+        {
           // S = Q K^T into S slot `slot`
           const uint32_t kb = sm_u32 + kSKV + slot * 2 * kTileKV;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint64_t bd = sw128_desc(kb + (j >> 2) * (kChunk * 128) + (j & 3) * 32, 1024);
-            mma_ts(tmem + kColS + 64 * slot, tmem + kColQ + 8 * j, bd, kIdQK, j > 0);
+            mma_ts(tmem_u + kColS + 64 * slot, tmem_u + kColQ + 8 * j, bd, kIdQK, j > 0);
           }
           mma_commit(bar_s + 8 * slot);
         }
@@ -492,56 +499,76 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
         }
       }
       if (nch > 0 && !dead && !issue_pv(kbase + (uint32_t)(nch - 1), nch == 1) && lane == 0) dead = 1;
-    } else if (producer) {
-      // ======== dequant warps: raw copies, raw stage -> swizzled K/V tiles ========
-      // Thread (token tt of the chunk, head_dim half hf) copies its own slice
-      // of each chunk (K and V half rows and their block scales) into the raw
-      // stage with cp.async, kRaw chunks ahead, and is the only thread that
-      // reads that slice back; a stage's mbarrier completes once all 128
-      // threads' copies have landed.  Absent tokens and bad pages zero-fill.
-      // A warp holds 16 consecutive tokens x both halves (lanes 0-15 half 0),
-      // so a quarter warp writes eight tokens' rows of one swizzled tile: no
-      // bank conflicts.
-      const int ptid = tid - 128, tt = ((ptid >> 5) << 4) | (ptid & 15), hf = (ptid >> 4) & 1;
-      auto page_of = [&](int c) -> int {
-        const int tok = c * kChunk + tt;
+    } else if (copy_warp) {
+      // ======== copy warps: raw K/V rows and block scales of each chunk ========
+      // Copy thread ct issues the copies of slices (token tt, half hf) number
+      // ct and ct + 64 in the dequant threads' numbering, into the same
+      // conflict-free raw layout; a stage is refilled once the four dequant
+      // warps have read it.  Absent tokens and bad pages zero-fill.
+      const int ct = tid - kCopyBase;
+      int ttj[2], hfj[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int p2 = ct + 64 * j;
+        ttj[j] = ((p2 >> 5) << 4) | (p2 & 15);
+        hfj[j] = (p2 >> 4) & 1;
+      }
+      auto page_of = [&](int c, int j) -> int {
+        const int tok = c * kChunk + ttj[j];
         return (c < c1 && tok < maxT) ? __ldg(prow + tok / a.P) : -1;
       };
-      auto fill = [&](int c, uint32_t st, int page) {
-        const int tok = c * kChunk + tt;
-        const bool in_seq = tok < maxT;
-        const bool ok = in_seq && page >= 0 && page < a.num_pages;
-        if (in_seq && !ok) pass_bad = 1;
-        const long long rowi = ok ? ((long long)page * a.H + h) * a.P + tok % a.P : 0;
+      int pg[2] = {page_of(c0, 0), page_of(c0, 1)};
+      for (int c = c0; c < c1; ++c) {
+        const uint32_t kk = kbase + (uint32_t)(c - c0), st = kk % Tr::kRaw;
+        bool ok = true;
+        if (kk >= (uint32_t)Tr::kRaw) ok = mbar_wait_bounded(bar_rfree + 8 * st, ((kk - Tr::kRaw) / Tr::kRaw) & 1u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) dead = 1;
+          break;
+        }
         const uint32_t stage = sm_u32 + kSRaw + st * Tr::kStage;
-        constexpr int kHalf = Tr::kRow / 2;
-        const uint8_t* sk = a.kd + rowi * Tr::kRow + hf * kHalf;
-        const uint8_t* sv = a.vd + rowi * Tr::kRow + hf * kHalf;
+        const int npg[2] = {page_of(c + 1, 0), page_of(c + 1, 1)};
 #pragma unroll
-        for (int i = 0; i < kHalf / 16; ++i) {
-          const uint32_t dk = stage + raw_off<F>(tt, hf, i);
-          cp_async16z(dk, sk + 16 * i, ok);
-          cp_async16z(dk + Tr::kData, sv + 16 * i, ok);
+        for (int j = 0; j < 2; ++j) {
+          const int tt = ttj[j], hf = hfj[j], page = pg[j];
+          const int tok = c * kChunk + tt;
+          const bool in_seq = tok < maxT;
+          const bool pok = in_seq && page >= 0 && page < a.num_pages;
+          if (in_seq && !pok) pass_bad = 1;
+          const long long rowi = pok ? ((long long)page * a.H + h) * a.P + tok % a.P : 0;
+          constexpr int kHalf = Tr::kRow / 2;
+          const uint8_t* sk = a.kd + rowi * Tr::kRow + hf * kHalf;
+          const uint8_t* sv = a.vd + rowi * Tr::kRow + hf * kHalf;
+#pragma unroll
+          for (int i = 0; i < kHalf / 16; ++i) {
+            const uint32_t dk = stage + raw_off<F>(tt, hf, i);
+            cp_async16z(dk, sk + 16 * i, pok);
+            cp_async16z(dk + Tr::kData, sv + 16 * i, pok);
+          }
+          if constexpr (Tr::kScales) {
+            const uint32_t ds = stage + 2 * Tr::kData + tt * 8 + hf * 4;
+            cp_async4z(ds, a.ks + rowi * 8 + hf * 4, pok);
+            cp_async4z(ds + Tr::kScl, a.vs + rowi * 8 + hf * 4, pok);
+          }
         }
-        if constexpr (Tr::kScales) {
-          const uint32_t ds = stage + 2 * Tr::kData + tt * 8 + hf * 4;
-          cp_async4z(ds, a.ks + rowi * 8 + hf * 4, ok);
-          cp_async4z(ds + Tr::kScl, a.vs + rowi * 8 + hf * 4, ok);
-        }
-        cp_async_arrive(bar_raw + 8 * st);
-      };
-      for (int c = c0; c < min(c0 + Tr::kRaw, c1); ++c)
-        fill(c, (kbase + (uint32_t)(c - c0)) % Tr::kRaw, page_of(c));
-      int next_page = page_of(c0 + Tr::kRaw);  // page of the chunk the next refill copies
+        // one pending arrival per thread, completed when its copies land; then
+        // one release arrival per copy warp (orders pass_bad before the stage)
+        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar_raw + 8 * st) : "memory");
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_raw + 8 * st) : "memory");
+        pg[0] = npg[0];
+        pg[1] = npg[1];
+      }
+    } else if (producer) {
+      // ======== dequant warps: raw stage -> swizzled K/V tiles ========
+      // Thread (token tt of the chunk, head_dim half hf) dequantizes its slice
+      // of K and V; a warp holds 16 consecutive tokens x both halves (lanes
+      // 0-15 half 0), so a quarter warp writes eight tokens' rows of one
+      // swizzled tile: no bank conflicts.
+      const int ptid = tid - 128, tt = ((ptid >> 5) << 4) | (ptid & 15), hf = (ptid >> 4) & 1;
       for (int c = c0; c < c1; ++c) {
         const uint32_t kk = kbase + (uint32_t)(c - c0), slot = kk % kSlots;
         const uint32_t rst = kk % Tr::kRaw;
-        // refill this thread's slice of the stage read in the previous
-        // iteration with chunk c - 1 + kRaw (issued before this chunk's work)
-        if (c > c0 && c - 1 + Tr::kRaw < c1) {
-          fill(c - 1 + Tr::kRaw, (kk - 1) % Tr::kRaw, next_page);
-          next_page = page_of(c + Tr::kRaw);
-        }
         // raw chunk landed; K/V slot and S slot free (PV of chunk kk - kSlots done)
         bool ok = mbar_wait_bounded(bar_raw + 8 * rst, (kk / Tr::kRaw) & 1u);
         if (ok && c - c0 >= kSlots) ok = mbar_wait_bounded(bar_o + 8 * slot, ((kk - kSlots) / kSlots) & 1u);
@@ -572,7 +599,10 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
         }
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_kv + 8 * slot) : "memory");
+        if (lane == 0) {
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_kv + 8 * slot) : "memory");
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_rfree + 8 * rst) : "memory");
+        }
       }
     } else {
       // ================= rows: online softmax, O rescale, epilogue =============
@@ -744,16 +774,17 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_kernel(ExtendArgs a) {
       a.part_lse[rowg * a.splits + split] = dead ? INFINITY : -INFINITY;
     }
   }
-  // after a wait ran out: give copies and MMAs still in flight a bounded
-  // chance to complete before the CTA frees its tensor memory and exits
+  // after a wait ran out: give MMAs still in flight a bounded chance to
+  // complete before the CTA frees its tensor memory and exits; every copy
+  // thread waits for its own copies
   if (dead && mma_warp) {
     const uint32_t k0 = k_next > kSlots ? k_next - kSlots : 0;
     for (uint32_t t = k0; t < k_next; ++t) {
-      mbar_wait_bounded(bar_raw + 8 * (t % Tr::kRaw), (t / Tr::kRaw) & 1u);
       mbar_wait_bounded(bar_s + 8 * (t % kSlots), (t / kSlots) & 1u);
       mbar_wait_bounded(bar_o + 8 * (t % kSlots), (t / kSlots) & 1u);
     }
   }
+  if (copy_warp) asm volatile("cp.async.wait_all;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
