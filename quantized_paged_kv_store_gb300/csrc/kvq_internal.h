@@ -70,7 +70,8 @@ cudaError_t launch_set_head_scales(float* scale, float* recip, const float* k, c
 
 // Calibration: amax over the finite values of bf16 K and V rows [n][H][D],
 // per kv head or per tensor, turned into scale = amax / fmt_max (1 if amax is
-// 0) and its reciprocal in scale / recip ([2][H]).  amax_scratch: 2 * H words.
+// 0) and its reciprocal in scale / recip ([2][H]).  amax_scratch: 2 * H words,
+// zero on entry and left zero (the calibration clears what it read).
 cudaError_t launch_calibrate(const Geometry& g, const void* k, const void* v, int n, bool per_head,
                              unsigned* amax_scratch, float* scale, float* recip,
                              cudaStream_t stream);

@@ -641,6 +641,7 @@ struct CalArgs {
   const uint16_t* x[2];  // K, V bf16 [n][H][D]
   int64_t n;
   int H, nb, hb;         // kv heads, 16-element blocks per row, H * nb
+  int fixed;             // the grid's thread count is a multiple of hb
   unsigned* amax;        // [2][H] bf16 magnitude bits of the largest finite |x|
 };
 
@@ -668,8 +669,27 @@ __global__ void __launch_bounds__(256) calib_amax_kernel(CalArgs a) {
   unsigned* const gmax = a.amax + (size_t)kv * a.H;
   const long long items = a.n * a.hb;
   const long long row = (long long)a.hb * 16;  // elements per token
-  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
-       it += (long long)gridDim.x * blockDim.x) {
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (a.fixed) {
+    // the thread's block column (head and block) is the same for every token
+    // it visits: keep the maximum in a register, one atomic at the end
+    const int pair = (int)(g % a.hb);
+    const long long tstep = (long long)gridDim.x * blockDim.x / a.hb;
+    const uint16_t* src = x + (g / a.hb) * row + (long long)pair * 16;
+    const long long sstep = tstep * row;
+    uint32_t m = 0u;
+#pragma unroll 4
+    for (long long tok = g / a.hb; tok < a.n; tok += tstep, src += sstep) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src);
+      m = max(m, block_amax_finite(__ldg(s4), __ldg(s4 + 1)));
+    }
+    const int h = pair / a.nb;
+    if (m != 0u) {
+      if (h < kCalSmemHeads) atomicMax(&smax[h], m);
+      else atomicMax(gmax + h, m);
+    }
+  }
+  for (long long it = a.fixed ? items : g; it < items; it += (long long)gridDim.x * blockDim.x) {
     const long long tok = it / a.hb;
     const int pair = (int)(it - tok * a.hb);
     const int h = pair / a.nb;
@@ -686,8 +706,9 @@ __global__ void __launch_bounds__(256) calib_amax_kernel(CalArgs a) {
 }
 
 // scale = amax / fmt_max (IEEE fp32 division), 1 when amax is 0; per tensor:
-// the largest amax over the heads serves every head.
-__global__ void __launch_bounds__(256) calib_finalize_kernel(const unsigned* amax, int H,
+// the largest amax over the heads serves every head.  The amax words are left
+// zero for the layer's next calibration (they start zero with the cache).
+__global__ void __launch_bounds__(256) calib_finalize_kernel(unsigned* amax, int H,
                                                              bool per_head, float fmt_max,
                                                              float* scale, float* recip) {
   __shared__ unsigned tmax[2];
@@ -703,6 +724,8 @@ __global__ void __launch_bounds__(256) calib_finalize_kernel(const unsigned* ama
     scale[i] = sc;
     recip[i] = 1.0f / sc;
   }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 2 * H; i += blockDim.x) amax[i] = 0u;
 }
 
 }  // namespace
@@ -733,8 +756,9 @@ cudaError_t launch_calibrate(const Geometry& g, const void* k, const void* v, in
   const float fmt_max = g.fmt == KVQ_FP8_E4M3 ? 448.0f
                         : g.fmt == KVQ_FP8_E5M2 ? 57344.0f
                                                 : 6.0f * 448.0f;  // NVFP4: E2M1 max x E4M3 max
-  cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned) * 2 * (size_t)g.kv_heads, stream);
-  if (e != cudaSuccess) return e;
+  // amax_scratch is zero here: zeroed with the cache, and again by every
+  // finalize after it has read it
+  cudaError_t e = cudaSuccess;
   CalArgs a;
   a.x[0] = static_cast<const uint16_t*>(k);
   a.x[1] = static_cast<const uint16_t*>(v);
@@ -745,7 +769,19 @@ cudaError_t launch_calibrate(const Geometry& g, const void* k, const void* v, in
   a.amax = amax_scratch;
   const int64_t items = (int64_t)n * a.hb;
   if (items > 0) {
-    dim3 grid(grid_for(items), 2);
+    // one resident wave of CTAs (K and V halves together), rounded down to a
+    // multiple of the CTA count whose threads span whole token rows (hb
+    // blocks each)
+    int dev = 0, sms = 148, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, calib_amax_kernel, 256, 0)) != cudaSuccess)
+      return e;
+    int64_t unit = a.hb;
+    for (int t = 0; t < 8 && unit % 2 == 0; ++t) unit /= 2;  // hb / gcd(hb, 256)
+    const int64_t ctas = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) / 2 / unit) * unit;
+    a.fixed = ctas <= 65535;
+    dim3 grid(a.fixed ? (unsigned)ctas : (unsigned)grid_for(items), 2);
     calib_amax_kernel<<<grid, 256, 0, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -143,6 +143,29 @@ def test_calibration_matches_oracle(kvq, orc, cuda, fmt, per_head):
         assert c.layer_scales(1) == (float(ref_k[0]), float(ref_v[0]))
 
 
+@pytest.mark.parametrize("fmt", ["fp8_e4m3", "nvfp4"])
+def test_calibration_many_tokens_odd_head_count(kvq, orc, cuda, fmt):
+    """3 kv heads x 4 blocks per row (12 block columns, not a divisor of a
+    CTA's 256 threads) over 40,000 tokens, more than one token per thread of
+    the calibration grid: every head's maximum (planted at scattered tokens,
+    beside non-finite values) is found."""
+    n, H, D = 40000, 3, 64
+    g = torch.Generator().manual_seed(17)
+    x = [synth.to_bf16_bits(torch.randn(n, H, D, generator=g) * torch.tensor([0.5, 8.0, 0.01]).view(1, H, 1))
+         for _ in range(2)]
+    for i, (t, h, d) in enumerate([(39999, 0, 63), (12345, 1, 0), (7, 2, 31)]):
+        x[0][t, h, d] = 0x4480 + i          # 1024 + i ulps: each head's largest K
+        x[1][n - 1 - t, h, d] = 0xC300 + i  # -128 - ...: each head's largest V
+    x[0][100, 1, 5] = 0x7F80
+    x[1][200, 2, 9] = 0xFFC0
+    c = kvq.KVQCache(fmt, 1, H, D, 16, 8)
+    c.calibrate_scales(0, bits_to_cuda(x[0]), bits_to_cuda(x[1]), True)
+    got_k, got_v = c.layer_head_scales(0)
+    ref_k, ref_v = orc.calibrate_scales(fmt, x[0], True), orc.calibrate_scales(fmt, x[1], True)
+    assert np.array_equal(np.float32(got_k), ref_k), (got_k, ref_k)
+    assert np.array_equal(np.float32(got_v), ref_v), (got_v, ref_v)
+
+
 def test_calibration_of_zeros_gives_one(kvq, cuda):
     c = kvq.KVQCache("fp8_e4m3", 1, 2, 32, 16, 2)
     z = torch.zeros(5, 2, 32, dtype=torch.bfloat16, device="cuda")
