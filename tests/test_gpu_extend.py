@@ -106,6 +106,37 @@ def test_extend_bad_rows_and_lengths(kvq, cuda):
     assert (got[1] == 0).all() and (got[3] != 0).any()
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "fp8_e4m3", "nvfp4"])
+@pytest.mark.parametrize("split", [False, True])
+def test_extend_bad_page_poisons_only_its_sequence(kvq, orc, cuda, fmt, split):
+    """A page id outside the pool in one sequence's page table: that
+    sequence's rows are zero and the device error word says
+    KVQ_ERR_DEVICE_RANGE; rows of the other sequences (some in the same CTA,
+    in other passes) still match the oracle.  With a workspace the context is
+    split and the poisoned partials are merged to zeros."""
+    wl = synth.make_workload(f"extbad_{fmt}", fmt, Hq=16, Hkv=4, seq_lens=[3000, 2600, 4100], seed=41)
+    c = gpu_cache_for(kvq, wl)
+    store_layer(c, wl)
+    q, q_seq, q_len = _queries(wl, [16, 16, 16], seed=6)
+    ref, rc = oracle_cache_for(orc, wl).extend_attention(q, q_seq, q_len, wl.page_table, wl.sm_scale)
+    assert rc == 0
+    pt = wl.page_table.copy()
+    pt[1, 40] = wl.num_pages + 5   # a page in the middle of sequence 1's context
+    ws = None
+    if split:
+        need = kvq.kvq_extend_workspace_size(c.handle, len(q_seq), wl.Hq, wl.max_pages)
+        assert need > 0
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = c.extend_attention(0, bits_to_cuda(q), torch.from_numpy(q_seq).cuda(), torch.from_numpy(q_len).cuda(),
+                             torch.from_numpy(pt).cuda(), wl.sm_scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert c.device_error() == kvq._binding._STATUS_CODES["KVQ_ERR_DEVICE_RANGE"]
+    got = synth.bf16_bits_to_float(cuda_to_bits(out)).astype(np.float64)
+    bad = q_seq == 1
+    assert (got[bad] == 0).all()
+    assert_attention_close(got[~bad], ref[~bad], f"{fmt} extend beside a bad page")
+
+
 @pytest.mark.parametrize("fmt", ["fp8_e4m3", "nvfp4"])
 def test_extend_split_and_unsplit_plans_agree(kvq, orc, cuda, fmt):
     """Long contexts: the fastest plan splits each sequence's context across
