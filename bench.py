@@ -49,6 +49,9 @@ DTYPE = {"bf16": "bf16 cache; bf16 mma, f32 accumulate",
 NCU_TRAFFIC = {("nvfp4", "c4e8e5df00bf1dc9"): 1091647038,
                ("fp4_mx_block16", "c4e8e5df00bf1dc9"): 1093249874}
 
+# steps between timed decode calls inside the timed step loop
+DECODE_SAMPLE = 8
+
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
@@ -460,8 +463,12 @@ def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True, with_extr
     if cache.device_error() != 0:
         raise RuntimeError("device error during warm-up: " + kvq.kvq_last_error_string())
     K = args.steps
-    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    # the decode call's own duration: a timing-event pair around it on every
+    # DECODE_SAMPLE-th step of the timed region (each pair costs the stream
+    # ~3.4 us, which a pair on every step would add to the step time)
+    sampled = list(range(0, K, DECODE_SAMPLE))
+    d0 = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
+    d1 = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -469,14 +476,16 @@ def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True, with_extr
         e_start.record(stream)
         for i in range(K):
             cache.quantize_and_store(0, d_k, d_v, d_slots, scales)
-            d0[i].record(stream)
+            if i in d0:
+                d0[i].record(stream)
             cache.decode_attention(0, d_q, d_pt, d_sl, wl.sm_scale, d_out, ws)
-            d1[i].record(stream)
+            if i in d1:
+                d1[i].record(stream)
         e_end.record(stream)
         torch.cuda.synchronize()
     barrier()
     local_ms = e_start.elapsed_time(e_end) / K
-    decode_ms = statistics.fmean(d0[i].elapsed_time(d1[i]) for i in range(K))
+    decode_ms = statistics.fmean(d0[i].elapsed_time(d1[i]) for i in sampled)
     if cache.device_error() != 0:
         raise RuntimeError("device error during the timed steps: " + kvq.kvq_last_error_string())
     dbytes = algorithmic_bytes(wl, fmt)
@@ -489,9 +498,9 @@ def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True, with_extr
         # same step through the public API with pinned host buffers: H2D of the
         # step's inputs, store + decode, D2H of the output, every step.  Steps
         # are pipelined the way a serving loop runs them: two sets of device
-        # buffers, the copies on their own stream, so that step i + 1's inputs
-        # go up and step i's output comes down while step i computes; the
-        # clock stops once every step's output is on the host.
+        # buffers, uploads and downloads each on their own stream, so that step
+        # i + 1's inputs go up and step i - 1's output comes down while step i
+        # computes; the clock stops once every step's output is on the host.
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
         h_k, h_v = pin(new_k.view(np.int16)), pin(new_v.view(np.int16))
         h_q = pin(q_h.view(np.int16))
@@ -504,33 +513,36 @@ def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True, with_extr
                      out=torch.empty_like(d_out)) for _ in range(NB)]
         h2d = sum(t.numel() * t.element_size() for t in (h_k, h_v, h_q, h_slots, h_pt, h_sl))
         d2h = h_out[0].numel() * h_out[0].element_size()
-        xs = torch.cuda.Stream()
-        ev_free = [torch.cuda.Event() for _ in range(NB)]
-        ev_in = [torch.cuda.Event() for _ in range(NB)]
-        for e in ev_free:
+        xs_in, xs_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_free = [torch.cuda.Event() for _ in range(NB)]   # the set's inputs are no longer read
+        ev_in = [torch.cuda.Event() for _ in range(NB)]     # the set's inputs are up
+        ev_out = [torch.cuda.Event() for _ in range(NB)]    # the set's output is down
+        for e in ev_free + ev_out:
             e.record(stream)
 
         def e2e_step(i):
             b = i % NB
             d = sets[b]
-            xs.wait_event(ev_free[b])  # the set's previous step has computed
-            with torch.cuda.stream(xs):
+            xs_in.wait_event(ev_free[b])  # the set's previous step has computed
+            with torch.cuda.stream(xs_in):
                 d["k"].copy_(h_k, non_blocking=True)
                 d["v"].copy_(h_v, non_blocking=True)
                 d["q"].copy_(h_q, non_blocking=True)
                 d["slots"].copy_(h_slots, non_blocking=True)
                 d["pt"].copy_(h_pt, non_blocking=True)
                 d["sl"].copy_(h_sl, non_blocking=True)
-            ev_in[b].record(xs)
+            ev_in[b].record(xs_in)
             stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])  # the set's previous output has been read
             cache.quantize_and_store(0, d["k"].view(torch.bfloat16), d["v"].view(torch.bfloat16), d["slots"],
                                      scales, stream=stream)
             cache.decode_attention(0, d["q"].view(torch.bfloat16), d["pt"], d["sl"], wl.sm_scale, d["out"], ws,
                                    stream=stream)
             ev_free[b].record(stream)
-            xs.wait_event(ev_free[b])
-            with torch.cuda.stream(xs):
+            xs_out.wait_event(ev_free[b])
+            with torch.cuda.stream(xs_out):
                 h_out[b].copy_(d["out"].view(torch.int16), non_blocking=True)
+            ev_out[b].record(xs_out)
 
         for i in range(max(3, args.warmup // 4)):
             e2e_step(i)
@@ -550,7 +562,7 @@ def run_cell(args, fmt, T=None, B=None, with_cpu=False, with_e2e=True, with_extr
         e2e_ms, e2e_gbs = aggregate(e2e_ms_local, dbytes + sbytes, dev)
         res["e2e"] = {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
-                      "pipelined": "two buffer sets; copies on their own stream overlap compute"}
+                      "pipelined": "two buffer sets; uploads and downloads on their own streams overlap compute"}
 
     if with_extra and rank == 0:
         # quantization error of the timed output against fp64 attention over the
