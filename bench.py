@@ -676,16 +676,7 @@ def run_store(args, steps=None, warmup=None):
         wl.fmt = fmt
         scales = [float(x) for x in wl._scales_from(ks, vs)]
         cache = kvq.KVQCache(fmt, 1, wl.Hkv, wl.D, wl.P, wl.num_pages)
-        for _ in range(warmup):
-            cache.quantize_and_store(0, k, v, slots, scales)
-        torch.cuda.synchronize()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-        ev[0].record()
-        for i in range(steps):
-            cache.quantize_and_store(0, k, v, slots, scales)
-            ev[i + 1].record()
-        torch.cuda.synchronize()
-        ms = statistics.fmean(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+        ms = _time_calls(lambda: cache.quantize_and_store(0, k, v, slots, scales), steps, warmup)
         if cache.device_error() != 0:
             raise RuntimeError("device error during the store benchmark")
         row_w = {"bf16": 256, "fp8_e4m3": 128, "fp8_e5m2": 128}.get(fmt, 64 + 8)
@@ -781,18 +772,20 @@ def run_sweep(args):
 
 
 def _time_calls(fn, steps, warmup):
-    """Mean CUDA-event milliseconds of fn() over `steps` calls after `warmup`."""
+    """Mean milliseconds per fn() call over `steps` back-to-back calls after
+    `warmup`: one CUDA-event pair on the launching stream around all of them
+    (a pair around every call would add its own stream cost, ~3.4 us, to each)."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    ev[0].record()
-    for i in range(steps):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
         fn()
-        ev[i + 1].record()
+    e1.record()
     torch.cuda.synchronize()
-    return statistics.fmean(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    return e0.elapsed_time(e1) / steps
 
 
 def run_next(args):
