@@ -133,11 +133,12 @@ __global__ void __launch_bounds__(kMergeMaxWarps * 32) merge_kernel(DecodeArgs a
 }  // namespace
 
 cudaError_t launch_merge(const DecodeArgs& a, int64_t num_units, cudaStream_t stream) {
-  // about four partials per warp on average (one batch of loads), 1 to 32
-  // warps per CTA
+  // about eight partials per warp on average (two batches of loads), 1 to 32
+  // warps per CTA; measured at batch 32 x 32K (about 11 partials per unit):
+  // two warps per CTA 0.8% faster per decode call than four, eight 1.6% slower
   const int64_t per_unit = (a.num_workers + num_units - 1) / num_units + 1;
   int warps = 1;
-  while (warps < kMergeMaxWarps && warps * 4 < per_unit) warps <<= 1;
+  while (warps < kMergeMaxWarps && warps * 8 < per_unit) warps <<= 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(num_units * kGroupMax));
   cfg.blockDim = dim3(32 * warps);
