@@ -8,11 +8,13 @@
 // 16-element block computed on the fly; NVFP4 with an fp32 global scale and an
 // FP8-E4M3 scale per block.
 //
-// One thread owns one 16-element block of one (token, kv_head) row: two
-// 16-byte loads of bf16, the block amax in registers, encode, and one 16-byte
-// (FP8) or 8-byte (FP4) store into the paged row plus one scale byte.  Eight
-// consecutive threads cover one 128-element row, so loads and stores of a warp
-// are contiguous 1 KB / 512 B / 256 B runs.  The kernel is HBM-bound.
+// One thread owns an item: one 16-element block of one (token, kv_head) row
+// (the bf16 copy) or two, blocks j and j + nb/2 of the row (the quantizing
+// formats).  Per block: two 16-byte loads of bf16, the block amax in
+// registers, encode, and one 16-byte (FP8) or 8-byte (FP4) store into the
+// paged row plus one scale byte.  Consecutive threads take consecutive items,
+// so a warp's loads and stores cover contiguous runs of each row half.  The
+// kernel is HBM-bound (NVFP4: bound by instruction issue).
 #include <algorithm>
 
 #include "kvq_codecs.cuh"
@@ -215,7 +217,7 @@ __device__ __forceinline__ void store_block(uint8_t* dat, uint8_t* scl, int64_t 
 // while it computes.  PH: the scale of each item's kv head comes from the
 // per-head arrays ("Quantized KV cache" (vLLM), Supported schemes:
 // per-attention-head scales) instead of the per-tensor launch argument.
-// BPI (blocks per item): the FP4 stores take two blocks of a row per item --
+// BPI (blocks per item): the quantizing formats take two blocks of a row per item --
 // block j and block j + nb / 2 of one head, so that each of a warp's loads
 // and stores covers consecutive blocks -- and share the slot, page and row
 // arithmetic and the loop bookkeeping between them.
